@@ -1,0 +1,389 @@
+"""Benchmark of the hot path: causal GQA prefill at the Llama-3-8B attention
+shape plus paged one-token decode, through the C ABI, on one GB300 per rank.
+
+One step = attn_fwd on the prefill workload, then attn_decode_paged on the
+decode workload (every row of the hot-path table runs once).  Inputs are
+seeded synthetic data (the generator in exact_attention_40_gb300.synth),
+resident in HBM before timing.  L2 is flushed (a 256 MiB write) before each
+step; the flush is outside the timed kernels.  Each kernel group is timed
+with CUDA events on the launching stream.
+
+Prints one JSON line (rank 0).  `value` is prefill TFLOP/s (causal FLOPs
+4*B*Hq*Nq*Nk*d/2 over the summed prefill kernel time, summed over ranks);
+decode HBM GB/s is reported under "decode".
+
+--impl reference times the fp64 CPU oracle on this host's cores instead,
+each step on a bounded sample of the same prefill workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_40_gb300 import synth  # noqa: E402
+
+PREFILL_CFG = synth.PREFILL["llama3_8b_causal"]
+DECODE_CFG = synth.DECODE["decode_paged"]
+WORKLOAD = ("prefill llama3_8b_causal (B1 Hq32 Hkv8 Nq=Nk=2048 d128 causal) + "
+            "paged decode (64 seqs, ctx U[512,8192], Hq32 Hkv8 d128, 16-token blocks)")
+METRIC = "attn fwd TFLOP/s & % BF16 tensor peak; paged decode GB/s & % HBM peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def load_traffic(kernel_file, key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel source as it is now (matched by SHA-256), else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "exact_attention_40_gb300", "csrc", kernel_file)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    ent = data.get(key)
+    if not ent:
+        return None
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    return ent.get("bytes_per_launch") if ent.get("source_sha256") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling for the duration of the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = "/tmp/exattn_clocks_%d_%d.csv" % (os.getpid(), gpu_index)
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(backend):
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def prefill_row_flops(rows, Nq, Nk, d, causal):
+    """Algorithmic FLOPs (4*d per visible score) of the given query rows."""
+    i = rows[:, 2].astype(np.int64)
+    vis = np.minimum(i + (Nk - Nq) + 1, Nk) if causal else np.full_like(i, Nk)
+    return float((4 * d * np.maximum(vis, 0)).sum())
+
+
+def run_reference(args):
+    """The oracle on the host cores, each step a bounded sample of the prefill workload."""
+    rank, world, _ = dist_setup("gloo")
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cfg = PREFILL_CFG
+    q, k, v = synth.prefill_inputs(cfg)
+    per_step_rows = max(8, min(1024, int(args.ref_rows_total) // max(1, args.steps + args.warmup)))
+    all_rows = synth.sample_rows(cfg.seed, cfg.B, cfg.Hq, cfg.N, 64)
+
+    def step(i):
+        sel = all_rows[(np.arange(per_step_rows) + i * per_step_rows) % len(all_rows)]
+        oracle.attn_rows(q, k, v, sel, cfg.scale, cfg.causal)
+        return prefill_row_flops(sel, cfg.N, cfg.N, cfg.d, cfg.causal)
+
+    for i in range(args.warmup):
+        step(i)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "%d query rows of the prefill per step" % per_step_rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d seeded query rows per step of the llama3_8b_causal prefill, "
+                                   "full fp64 rows over all visible keys" % per_step_rows},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline_leg():
+    """Oracle on this host's cores over a bounded sample (about 10-30 s)."""
+    import oracle
+    oracle.build()
+    cfg = PREFILL_CFG
+    q, k, v = synth.prefill_inputs(cfg)
+    rows = synth.sample_rows(cfg.seed + 100, cfg.B, cfg.Hq, cfg.N, 16)
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, rows, cfg.scale, cfg.causal)
+    dt = time.perf_counter() - t0
+    fl = prefill_row_flops(rows, cfg.N, cfg.N, cfg.d, cfg.causal)
+    # scale the sample so the leg takes roughly 10 s
+    reps = int(max(1, min(64, 10.0 / max(dt, 1e-3))))
+    rows = synth.sample_rows(cfg.seed + 100, cfg.B, cfg.Hq, cfg.N, min(cfg.N, 16 * reps))
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, rows, cfg.scale, cfg.causal)
+    dt = time.perf_counter() - t0
+    fl = prefill_row_flops(rows, cfg.N, cfg.N, cfg.d, cfg.causal)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": "%d seeded query rows (%d per head) of the llama3_8b_causal prefill, "
+                      "fp64, full score rows" % (len(rows), len(rows) // cfg.Hq)}
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from exact_attention_40_gb300 import build
+    build.build()
+    from exact_attention_40_gb300 import exattn
+
+    peaks = load_peaks()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    # ---- inputs resident in HBM
+    pc = PREFILL_CFG
+    q_np, k_np, v_np = synth.prefill_inputs(pc)
+    q, k, v = to_dev(q_np), to_dev(k_np), to_dev(v_np)
+    out = torch.empty_like(q)
+    lse = torch.empty((pc.B, pc.Hq, pc.N), device=dev, dtype=torch.float32)
+    dc = DECODE_CFG
+    dinp = synth.decode_inputs(dc)
+    dq, dk, dv = to_dev(dinp["q"]), to_dev(dinp["k_cache"]), to_dev(dinp["v_cache"])
+    dbt, dcl = to_dev(dinp["block_table"]), to_dev(dinp["ctx_lens"])
+    dout = torch.empty_like(dq)
+    dlse = torch.empty((dc.num_seqs, dc.Hq), device=dev, dtype=torch.float32)
+    ws = torch.empty(exattn.attn_decode_workspace_bytes(dc.num_seqs, dc.Hq, dc.d,
+                                                        dinp["block_table"].shape[1]),
+                     device=dev, dtype=torch.uint8)
+    flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    prefill_flops = pc.flops()
+    decode_bytes = synth.decode_kv_bytes(dinp["ctx_lens"], dc.Hkv, dc.d)
+    decode_bytes_all = decode_bytes + 2 * dinp["q"].nbytes + dinp["block_table"].nbytes + \
+        dinp["ctx_lens"].nbytes + dc.num_seqs * dc.Hq * 4
+
+    def step(ev):
+        flush.fill_(1)
+        ev[0].record(stream)
+        exattn.attn_fwd(q, k, v, causal=True, out=out, lse=lse)
+        ev[1].record(stream)
+        exattn.attn_decode_paged(dq, dk, dv, dbt, dcl, out=dout, lse=dlse, workspace=ws)
+        ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize()
+    if exattn.attn_get_device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        step(events[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    status = exattn.attn_get_device_status()
+    if status != 0:
+        raise RuntimeError("device status word %#x after the timed region" % status)
+
+    pre_ms = [events[i][0].elapsed_time(events[i][1]) for i in range(args.steps)]
+    dec_ms = [events[i][1].elapsed_time(events[i][2]) for i in range(args.steps)]
+    pre_total = max_over_ranks(sum(pre_ms), world, dev)
+    dec_total = max_over_ranks(sum(dec_ms), world, dev)
+    value = world * args.steps * prefill_flops / (pre_total * 1e-3) / 1e12
+    dec_gbs = world * args.steps * decode_bytes / (dec_total * 1e-3) / 1e9
+    pre_avg_ms = pre_total / args.steps
+    dec_avg_ms = dec_total / args.steps
+    achieved = prefill_flops / (pre_avg_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hq_ = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hk_ = torch.from_numpy(k_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hv_ = torch.from_numpy(v_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        ho = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(hq_, non_blocking=True)
+            kd.copy_(hk_, non_blocking=True)
+            vd.copy_(hv_, non_blocking=True)
+            exattn.attn_fwd(qd, kd, vd, causal=True, out=out, lse=lse)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": world * args.e2e_steps * prefill_flops / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "steps": args.e2e_steps,
+               "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
+               "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4}
+
+    if rank != 0:
+        return 0
+    cpu = None if args.no_cpu_baseline else cpu_baseline_leg()
+    traffic = load_traffic("prefill.cu", "prefill_llama3_8b_causal")
+    dtraffic = load_traffic("decode.cu", "decode_split_decode_paged")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (pre_total + dec_total) / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed before every step (256 MiB write, outside the timed kernels)",
+                   "wall_s_timed_region": t_wall},
+        "prefill": {"tflops": achieved, "ms": pre_avg_ms,
+                    "frac_bf16_peak": achieved / peaks["bf16"], "flops": prefill_flops},
+        "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_avg_ms,
+                   "frac_hbm_peak": dec_gbs / world / peaks["hbm"],
+                   "frac_8tbs": dec_gbs / world / 8000.0,
+                   "kv_bytes": decode_bytes, "all_bytes": decode_bytes_all},
+        "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": achieved,
+                     "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                     "peak_kind": "bf16 burst (%s)" % peaks["src"], "traffic": traffic},
+        "roofline_decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
+                            "bound": "hbm", "achieved": decode_bytes / (dec_avg_ms * 1e-3) / 1e9,
+                            "peak": peaks["hbm"], "unit": "GB/s",
+                            "frac": decode_bytes / (dec_avg_ms * 1e-3) / 1e9 / peaks["hbm"],
+                            "peak_kind": "HBM copy (%s)" % peaks["src"], "traffic": dtraffic},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="exattn", choices=["exattn", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows-total", type=int, default=60000,
+                    help="reference arm: query rows spread over all steps")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

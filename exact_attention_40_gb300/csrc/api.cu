@@ -1,0 +1,304 @@
+// C ABI of libexattn.so (declared in include/exattn.h): argument checks,
+// TMA descriptor encoding and caching, the device status word, launches.
+//
+// Every check runs on the host before any CUDA call, so a rejected call
+// touches no GPU state.  Nothing here allocates device memory: the status
+// word is a static device variable, and decode scratch is the caller's.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/exattn.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace {
+
+__device__ unsigned int g_status_word;  // OR of EXATTN_DEVICE_*_BIT, one per GPU
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct MapKey {
+  uintptr_t ptr;
+  int d;
+  long long rows;
+  long long planes;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && d == o.d && rows == o.rows && planes == o.planes;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+    h ^= (static_cast<uint64_t>(k.d) << 1) + static_cast<uint64_t>(k.rows) * 0xBF58476D1CE4E5B9ull;
+    h ^= static_cast<uint64_t>(k.planes) * 0x94D049BB133111EBull;
+    return static_cast<size_t>(h ^ (h >> 31));
+  }
+};
+constexpr size_t kMapCacheMax = 4096;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps[kMaxDevices];
+
+unsigned long long wait_budget_ns() {
+  static const unsigned long long v = [] {
+    const char* e = std::getenv("EXATTN_WAIT_TIMEOUT_NS");
+    unsigned long long x = e ? std::strtoull(e, nullptr, 10) : 0ull;
+    return x > 0 ? x : 2000000000ull;  // 2 s: far beyond any legitimate pipeline wait
+  }();
+  return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Current device, its status-word address and the encode entry point.
+// Caller holds g_mu.
+int device_state(int* dev, unsigned int** status) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return EXATTN_ERR_CUDA;
+  if (g_status_ptr[*dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return EXATTN_ERR_CUDA;
+    g_status_ptr[*dev] = static_cast<unsigned int*>(p);
+  }
+  *status = g_status_ptr[*dev];
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return EXATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return EXATTN_OK;
+}
+
+// Descriptor of a bf16 tensor viewed as [planes, rows, d] (d innermost),
+// loaded/stored in boxes of 128 rows x 64 columns with 128-byte swizzle;
+// rows past `rows` read as zero and are not written.  Caller holds g_mu.
+int tensor_map(int dev, const void* ptr, int d, long long rows, long long planes,
+               const CUtensorMap** out) {
+  const MapKey key{reinterpret_cast<uintptr_t>(ptr), d, rows, planes};
+  auto& cache = g_maps[dev];
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = &it->second;
+    return EXATTN_OK;
+  }
+  if (cache.size() >= kMapCacheMax) cache.clear();
+  CUtensorMap m;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return EXATTN_ERR_CUDA;
+  auto ins = cache.emplace(key, m);
+  *out = &ins.first->second;
+  return EXATTN_OK;
+}
+
+// One warp waits on a barrier with arrival count 2 that only ever sees one
+// arrival, so the phase never completes and the bounded wait must expire.
+__global__ void expire_wait_kernel(unsigned int* status, unsigned long long budget_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    exattn::mbar_init(&bar, 2);
+    exattn::fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) exattn::mbar_arrive(&bar);
+  const bool done = exattn::mbar_wait(&bar, 0, budget_ns);
+  if (!__all_sync(0xffffffffu, done) && threadIdx.x == 0) atomicOr(status, EXATTN_DEVICE_TIMEOUT_BIT);
+}
+
+bool good_scale(float s) { return std::isfinite(s) && s > 0.f; }
+
+int decode_max_splits(int max_blocks_per_seq, int block_size) {
+  const long long tokens = static_cast<long long>(max_blocks_per_seq) * block_size;
+  return static_cast<int>((tokens + exattn::kDecodeSplitTokens - 1) / exattn::kDecodeSplitTokens);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case EXATTN_OK: return "EXATTN_OK";
+    case EXATTN_ERR_INVALID_ARG: return "EXATTN_ERR_INVALID_ARG";
+    case EXATTN_ERR_UNSUPPORTED: return "EXATTN_ERR_UNSUPPORTED";
+    case EXATTN_ERR_ALIGNMENT: return "EXATTN_ERR_ALIGNMENT";
+    case EXATTN_ERR_WORKSPACE: return "EXATTN_ERR_WORKSPACE";
+    case EXATTN_ERR_CUDA: return "EXATTN_ERR_CUDA";
+    case EXATTN_ERR_TIMEOUT: return "EXATTN_ERR_TIMEOUT";
+    case EXATTN_ERR_DEVICE_BOUNDS: return "EXATTN_ERR_DEVICE_BOUNDS";
+    default: return "EXATTN_UNKNOWN_STATUS";
+  }
+}
+
+int attn_decode_split_tokens(void) { return exattn::kDecodeSplitTokens; }
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0) return EXATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !good_scale(scale)) return EXATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return EXATTN_ERR_UNSUPPORTED;
+  if (Nq > (1 << 30) || Nk > (1 << 30) || B > 65535 || Hq > 65535 ||
+      static_cast<long long>(B) * Hq > 0x7FFFFFFFll)
+    return EXATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Nq == 0) return EXATTN_OK;
+  if (q == nullptr || out == nullptr || (Nk > 0 && (k == nullptr || v == nullptr)))
+    return EXATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || (Nk > 0 && (!aligned16(k) || !aligned16(v))) ||
+      (lse != nullptr && !aligned4(lse)))
+    return EXATTN_ERR_ALIGNMENT;
+
+  exattn::PrefillArgs a;
+  exattn::DeviceGuard g;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    int rc = device_state(&dev, &g.status);
+    if (rc != EXATTN_OK) return rc;
+    const long long pq = static_cast<long long>(B) * Hq, pk = static_cast<long long>(B) * Hkv;
+    if ((rc = tensor_map(dev, q, d, Nq, pq, &a.tm_q)) != EXATTN_OK) return rc;
+    if ((rc = tensor_map(dev, out, d, Nq, pq, &a.tm_o)) != EXATTN_OK) return rc;
+    if (Nk > 0) {
+      if ((rc = tensor_map(dev, k, d, Nk, pk, &a.tm_k)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, v, d, Nk, pk, &a.tm_v)) != EXATTN_OK) return rc;
+    } else {
+      a.tm_k = a.tm_q;  // never dereferenced: no key tiles exist
+      a.tm_v = a.tm_q;
+    }
+    g.wait_ns = wait_budget_ns();
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.causal = causal ? 1 : 0;
+    a.scale = scale;
+    // Launch while holding the lock: the descriptors are copied into the
+    // kernel's parameters at launch, so a concurrent cache eviction cannot
+    // invalidate them afterwards.
+    if (exattn::launch_prefill(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return EXATTN_ERR_CUDA;
+  }
+  return EXATTN_OK;
+}
+
+size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_per_seq,
+                                   int block_size) {
+  if (num_seqs < 0 || Hq < 1 || (d != 64 && d != 128) || max_blocks_per_seq < 1 ||
+      block_size != exattn::kDecodeBlockSize)
+    return 0;
+  const size_t splits = static_cast<size_t>(decode_max_splits(max_blocks_per_seq, block_size));
+  const size_t rows = static_cast<size_t>(num_seqs) * Hq * splits;
+  const size_t o_bytes = rows * d * sizeof(float);
+  const size_t lse_bytes = (rows * sizeof(float) + 15) & ~static_cast<size_t>(15);
+  return o_bytes + lse_bytes;
+}
+
+int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
+                      int num_seqs, int Hq, int Hkv, int d, int block_size, int num_blocks,
+                      int max_blocks_per_seq, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (num_seqs < 0 || Hq < 1 || Hkv < 1 || num_blocks < 0 || max_blocks_per_seq < 1)
+    return EXATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !good_scale(scale)) return EXATTN_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || block_size != exattn::kDecodeBlockSize) return EXATTN_ERR_UNSUPPORTED;
+  const int group = Hq / Hkv;
+  const long long ychunks = static_cast<long long>(Hkv) * ((group + 3) / 4);
+  if (num_seqs > 65535 || Hq > 65535 || ychunks > 65535 ||
+      static_cast<long long>(max_blocks_per_seq) * block_size > (1 << 30))
+    return EXATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return EXATTN_OK;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
+      ctx_lens == nullptr || out == nullptr)
+    return EXATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned4(block_table) || !aligned4(ctx_lens) || (lse != nullptr && !aligned4(lse)))
+    return EXATTN_ERR_ALIGNMENT;
+  const size_t need = attn_decode_workspace_bytes(num_seqs, Hq, d, max_blocks_per_seq, block_size);
+  if (workspace == nullptr || workspace_bytes < need) return EXATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXATTN_ERR_ALIGNMENT;
+
+  exattn::DecodeArgs a;
+  exattn::DeviceGuard g;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    const int rc = device_state(&dev, &g.status);
+    if (rc != EXATTN_OK) return rc;
+  }
+  g.wait_ns = wait_budget_ns();
+  const int splits = decode_max_splits(max_blocks_per_seq, block_size);
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.ctx_lens = ctx_lens;
+  a.out = out;
+  a.lse = lse;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                      static_cast<size_t>(num_seqs) * Hq * splits * d * sizeof(float));
+  a.num_seqs = num_seqs;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.num_blocks = num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_splits = splits;
+  a.scale = scale;
+  if (exattn::launch_decode(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXATTN_ERR_CUDA;
+  return EXATTN_OK;
+}
+
+int attn_get_device_status(void* stream, unsigned int* status_out) {
+  if (status_out == nullptr) return EXATTN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return EXATTN_ERR_CUDA;
+  *status_out = v;
+  return EXATTN_OK;
+}
+
+int attn_debug_expire_wait(unsigned long long budget_ns, void* stream) {
+  if (budget_ns < 1ull || budget_ns > 10000000000ull) return EXATTN_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    const int rc = device_state(&dev, &status);
+    if (rc != EXATTN_OK) return rc;
+  }
+  expire_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, budget_ns);
+  return cudaGetLastError() == cudaSuccess ? EXATTN_OK : EXATTN_ERR_CUDA;
+}
+
+void attn_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& m : g_maps) m.clear();
+}
+
+}  // extern "C"

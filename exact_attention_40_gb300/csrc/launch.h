@@ -1,0 +1,50 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace exattn {
+
+// Wait budget for every bounded pipeline wait inside the kernels.
+struct DeviceGuard {
+  unsigned int* status;        // device status word (OR of EXATTN_DEVICE_*_BIT)
+  unsigned long long wait_ns;  // per-wait time budget
+};
+
+struct PrefillArgs {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  const CUtensorMap* tm_o;
+  float* lse;
+  int B, Hq, Hkv, Nq, Nk, d;
+  int causal;
+  float scale;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t stream);
+size_t prefill_smem_bytes(int d);
+
+constexpr int kDecodeSplitTokens = 512;
+constexpr int kDecodeBlockSize = 16;
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  void* out;
+  float* lse;
+  float* ws_o;    // [num_seqs, Hq, max_splits, d]
+  float* ws_lse;  // [num_seqs, Hq, max_splits]
+  int num_seqs, Hq, Hkv, d, num_blocks, max_blocks_per_seq, max_splits;
+  float scale;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t stream);
+
+}  // namespace exattn

@@ -1,0 +1,184 @@
+"""Thin ctypes binding of libexattn.so (C ABI in include/exattn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the stream.
+Importing this module loads the library and raises if it has not been
+built (``python -m exact_attention_40_gb300.build``) -- there is no
+fallback path.
+
+The functions carry the C names.  ``attn_fwd`` and ``attn_decode_paged``
+take torch tensors, allocate outputs when none are given, and raise
+``ExattnError`` on a non-zero status.  ``lib`` is the raw ctypes handle for
+callers (and tests) that pass pointers themselves.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libexattn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libexattn.so is not built (%s); run `python -m exact_attention_40_gb300.build`" % LIB_PATH)
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+lib.attn_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P]
+lib.attn_fwd.restype = _I
+lib.attn_decode_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+lib.attn_decode_workspace_bytes.restype = _SZ
+lib.attn_decode_paged.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P,
+                                  _SZ, _P]
+lib.attn_decode_paged.restype = _I
+lib.attn_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
+lib.attn_get_device_status.restype = _I
+lib.attn_status_string.argtypes = [_I]
+lib.attn_status_string.restype = ctypes.c_char_p
+lib.attn_decode_split_tokens.argtypes = []
+lib.attn_decode_split_tokens.restype = _I
+lib.attn_debug_expire_wait.argtypes = [ctypes.c_ulonglong, _P]
+lib.attn_debug_expire_wait.restype = _I
+lib.attn_shutdown.argtypes = []
+lib.attn_shutdown.restype = None
+
+EXATTN_OK = 0
+DEVICE_TIMEOUT_BIT = 1
+DEVICE_BOUNDS_BIT = 2
+
+
+class ExattnError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__("%s failed: %s" % (fn, attn_status_string(status)))
+        self.status = status
+
+
+def attn_status_string(status: int) -> str:
+    return lib.attn_status_string(int(status)).decode()
+
+
+def attn_decode_split_tokens() -> int:
+    return lib.attn_decode_split_tokens()
+
+
+def attn_decode_workspace_bytes(num_seqs, Hq, d, max_blocks_per_seq, block_size=16) -> int:
+    return int(lib.attn_decode_workspace_bytes(num_seqs, Hq, d, max_blocks_per_seq, block_size))
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensor(name, t, dtype, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must live on a CUDA device" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() != ndim:
+        raise ValueError("%s must have %d dimensions, got %d" % (name, ndim, t.dim()))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             return_lse: bool = True, stream=None):
+    """Prefill attention.  q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d], bf16, contiguous.
+
+    Returns (out [B,Hq,Nq,d] bf16, lse [B,Hq,Nq] fp32 or None)."""
+    import torch
+    _check_tensor("q", q, torch.bfloat16, 4)
+    _check_tensor("k", k, torch.bfloat16, 4)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or dk != d:
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_tensor("out", out, torch.bfloat16, 4)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
+    elif lse is not None:
+        _check_tensor("lse", lse, torch.float32, 3)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Nq, Nk, d,
+                          float(scale), int(bool(causal)), _stream_handle(stream))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_fwd", rc)
+    return out, lse
+
+
+def attn_decode_paged(q, k_cache, v_cache, block_table, ctx_lens, scale: float | None = None,
+                      out=None, lse=None, workspace=None, return_lse: bool = True, stream=None):
+    """One-token decode.  q [S,Hq,d]; caches [num_blocks,Hkv,16,d] bf16;
+    block_table int32 [S,max_blocks]; ctx_lens int32 [S].
+
+    Returns (out [S,Hq,d] bf16, lse [S,Hq] fp32 or None)."""
+    import torch
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("k_cache", k_cache, torch.bfloat16, 4)
+    _check_tensor("v_cache", v_cache, torch.bfloat16, 4)
+    _check_tensor("block_table", block_table, torch.int32, 2)
+    _check_tensor("ctx_lens", ctx_lens, torch.int32, 1)
+    S, Hq, d = q.shape
+    num_blocks, Hkv, bs, dk = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or dk != d or block_table.shape[0] != S \
+            or ctx_lens.shape[0] != S:
+        raise ValueError("shape mismatch")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((S, Hq), device=q.device, dtype=torch.float32)
+    need = attn_decode_workspace_bytes(S, Hq, d, max_blocks, bs)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   block_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr() if lse is not None else None, S, Hq, Hkv, d, bs,
+                                   num_blocks, max_blocks, float(scale), workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(),
+                                   _stream_handle(stream))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_decode_paged", rc)
+    return out, lse
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device status word."""
+    v = ctypes.c_uint(0)
+    rc = lib.attn_get_device_status(_stream_handle(stream), ctypes.byref(v))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_get_device_status", rc)
+    return int(v.value)
+
+
+def attn_debug_expire_wait(budget_ns: int, stream=None) -> None:
+    """Launch the diagnostic kernel whose bounded wait must run out."""
+    rc = lib.attn_debug_expire_wait(int(budget_ns), _stream_handle(stream))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_debug_expire_wait", rc)
+
+
+def attn_shutdown() -> None:
+    lib.attn_shutdown()

@@ -23,6 +23,7 @@ a block table (same page, Paged Attention section).
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass
 
 import numpy as np
@@ -65,27 +66,46 @@ def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def normal_bf16(seed: int, tid: int, shape, chunk: int = 1 << 24) -> np.ndarray:
-    """i.i.d. N(0,1) values rounded to bf16, as uint16 bit patterns."""
+def _normal_pairs(stream: int, first_pair: int, npairs: int) -> np.ndarray:
+    """Box-Muller on SplitMix64 pairs first_pair .. first_pair+npairs-1, fp64."""
+    z = splitmix64(stream, 2 * npairs, 2 * first_pair)
+    u1 = ((z[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+    u2 = (z[1::2] >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    r = np.sqrt(-2.0 * np.log(u1))
+    ang = 2.0 * math.pi * u2
+    pair = np.empty(2 * npairs, np.float64)
+    pair[0::2] = r * np.cos(ang)
+    pair[1::2] = r * np.sin(ang)
+    return pair
+
+
+def normal_bf16(seed: int, tid: int, shape, chunk: int = 1 << 21) -> np.ndarray:
+    """i.i.d. N(0,1) values rounded to bf16, as uint16 bit patterns.
+
+    Chunks of the counter stream are independent, so they are evaluated on
+    a thread pool; the result does not depend on the chunking."""
+    from concurrent.futures import ThreadPoolExecutor
+
     n = int(np.prod(shape))
     out = np.empty(n, np.uint16)
     stream = seed * 16 + tid
     npair = (n + 1) // 2
-    done = 0
-    while done < npair:
-        m = min(chunk, npair - done)
-        z = splitmix64(stream, 2 * m, 2 * done)
-        u1 = ((z[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
-        u2 = (z[1::2] >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
-        r = np.sqrt(-2.0 * np.log(u1))
-        ang = 2.0 * math.pi * u2
-        pair = np.empty(2 * m, np.float64)
-        pair[0::2] = r * np.cos(ang)
-        pair[1::2] = r * np.sin(ang)
-        lo = 2 * done
+
+    def work(first):
+        m = min(chunk, npair - first)
+        pair = _normal_pairs(stream, first, m)
+        lo = 2 * first
         hi = min(n, lo + 2 * m)
         out[lo:hi] = f32_to_bf16_bits(pair[: hi - lo].astype(np.float32))
-        done += m
+
+    starts = list(range(0, npair, chunk))
+    if len(starts) <= 1:
+        for st in starts:
+            work(st)
+    else:
+        workers = min(len(starts), max(1, (os.cpu_count() or 1)))
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(work, starts))
     return out.reshape(shape)
 
 

@@ -1,0 +1,148 @@
+/*
+ * exattn.h -- C ABI of libexattn.so: exact fused scaled-dot-product
+ * attention for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Fused Kernel Compiler" page, subsection FlashAttention
+ * Integration, equation Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V):
+ *
+ *     s_ij  = scale * <q_i, k_j>, with s_ij = -inf where the causal mask
+ *             hides key j;
+ *     o_i   = sum_j softmax_j(s_i.) v_j;
+ *     lse_i = log sum_j exp(s_ij)              (natural logarithm).
+ *
+ * It is computed in one pass with an online (running) softmax, so the score
+ * and probability matrices never exist in device memory (same subsection,
+ * items 1-4; "Kernel Fusion, Softmax, and Attention" page, attention
+ * paragraph).  Results equal the definition up to floating-point rounding
+ * order ("Optimizing LLM Inference ..." page, section The Shift Toward
+ * Efficient Inference Architectures).
+ *
+ * Conventions shared by every entry point:
+ *   - q, k, v, out, caches: bf16 (IEEE bfloat16), row-major, device memory,
+ *     base addresses 16-byte aligned.  lse: fp32, device memory.
+ *   - GQA: query head hq reads key/value head hq / (Hq / Hkv); Hq must be a
+ *     multiple of Hkv.
+ *   - Causal mask, aligned bottom-right: query row i sees key j iff
+ *     j <= i + (Nk - Nq).  A row that sees no key gets o = 0, lse = -inf.
+ *   - d (head dimension) is 64 or 128.  scale must be finite and > 0
+ *     (callers usually pass 1/sqrt(d)).
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous on that stream: validation happens on the host before
+ *     anything is enqueued; nothing synchronises.
+ *   - Ownership: the caller owns every buffer.  The library allocates no
+ *     device memory per call; it keeps one 4-byte device status word per
+ *     GPU (a static device variable) and a host-side cache of TMA tensor
+ *     descriptors.
+ *   - Errors: a non-zero return means nothing was launched (except
+ *     EXATTN_ERR_CUDA, returned when a launch itself failed).  Faults found
+ *     on the device (a bounded wait that ran out, a block-table entry out of
+ *     range) never trap: the kernel records them in the status word and
+ *     returns; read them with attn_get_device_status().
+ */
+#ifndef EXATTN_H_
+#define EXATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EXATTN_OK = 0,
+  EXATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, Hq % Hkv != 0, bad scale */
+  EXATTN_ERR_UNSUPPORTED = 2, /* d not in {64,128}, block_size != 16, size beyond limits */
+  EXATTN_ERR_ALIGNMENT = 3,   /* a device pointer not 16-byte aligned */
+  EXATTN_ERR_WORKSPACE = 4,   /* decode workspace missing or too small */
+  EXATTN_ERR_CUDA = 5,        /* a CUDA runtime/driver call or launch failed */
+  EXATTN_ERR_TIMEOUT = 6,     /* a bounded device wait ran out (reported as EXATTN_DEVICE_TIMEOUT_BIT) */
+  EXATTN_ERR_DEVICE_BOUNDS = 7 /* table entry / ctx_len out of range (EXATTN_DEVICE_BOUNDS_BIT) */
+} exattn_status;
+
+/* Device status word bits (attn_get_device_status). */
+#define EXATTN_DEVICE_TIMEOUT_BIT (1u << 0)
+#define EXATTN_DEVICE_BOUNDS_BIT (1u << 1)
+
+/*
+ * Prefill attention (causal or not, with GQA).
+ *   q    [B, Hq,  Nq, d] bf16      k, v [B, Hkv, Nk, d] bf16
+ *   out  [B, Hq,  Nq, d] bf16      lse  [B, Hq, Nq] fp32, may be NULL
+ * B, Hq, Hkv >= 1; Nq, Nk >= 0 (Nq == 0 or B == 0 is a no-op; Nk == 0
+ * gives o = 0, lse = -inf).  Nq, Nk <= 2^30; B*Hq, B*Hkv <= 2^31 - 1.
+ * Computes exactly one kernel launch.  Deterministic (no atomics on
+ * outputs).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int Nq, int Nk, int d, float scale, int causal, void* stream);
+
+/*
+ * Bytes of caller-provided device workspace attn_decode_paged needs: the
+ * split-KV partial outputs (fp32 [num_seqs, Hq, max_splits, d]) and their
+ * log-sum-exps (fp32 [num_seqs, Hq, max_splits]), where max_splits =
+ * ceil(max_blocks_per_seq * block_size / split_tokens).  Returns 0 for
+ * invalid arguments.
+ */
+size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_per_seq,
+                                   int block_size);
+
+/*
+ * One-token decode over a block-paged KV cache ("Optimizing LLM Inference
+ * ..." page, section Paged Attention and Dynamic KV Cache Management: the
+ * cache is cut into fixed-size blocks and a block table maps each
+ * sequence's logical token order to physical blocks).
+ *   q        [num_seqs, Hq, d] bf16 (one query token per sequence)
+ *   k_cache, v_cache [num_blocks, Hkv, block_size, d] bf16
+ *   block_table int32 [num_seqs, max_blocks_per_seq]: physical block of
+ *            logical block b of sequence s (entries past the last used
+ *            block are not read)
+ *   ctx_lens int32 [num_seqs]: cached tokens of sequence s, the current
+ *            token included; all of them are visible (no mask)
+ *   out      [num_seqs, Hq, d] bf16;  lse [num_seqs, Hq] fp32, may be NULL
+ *   workspace/workspace_bytes: device scratch of at least
+ *            attn_decode_workspace_bytes(...) bytes, 16-byte aligned;
+ *            its contents need not be initialised and are clobbered.
+ * block_size must be 16.  The key/value sweep of each sequence is cut into
+ * splits of split_tokens (512) tokens; each split yields a partial output
+ * and log-sum-exp, and a second kernel merges them (exact up to rounding).
+ * Two kernel launches.  A ctx_len of 0 gives o = 0, lse = -inf; a
+ * ctx_len above max_blocks_per_seq * block_size or a table entry outside
+ * [0, num_blocks) is clamped/skipped and flagged in the device status word.
+ */
+int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
+                      int num_seqs, int Hq, int Hkv, int d, int block_size, int num_blocks,
+                      int max_blocks_per_seq, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the status word of the
+ * current device: 0, or an OR of EXATTN_DEVICE_*_BIT.  Returns EXATTN_OK
+ * or EXATTN_ERR_CUDA.
+ */
+int attn_get_device_status(void* stream, unsigned int* status_out);
+
+/* Human-readable name of an exattn_status value (static string). */
+const char* attn_status_string(int status);
+
+/* Split size, in tokens, used by attn_decode_paged (a multiple of 16). */
+int attn_decode_split_tokens(void);
+
+/*
+ * Diagnostic for the failure path.  Launches one CTA that waits, through the
+ * same bounded mbarrier wait the attention kernels use, on a barrier that
+ * nothing ever completes.  After budget_ns nanoseconds (1 .. 10^10) the wait
+ * gives up, the kernel sets EXATTN_DEVICE_TIMEOUT_BIT in the status word and
+ * returns; the GPU context stays usable.  Returns EXATTN_OK once launched.
+ */
+int attn_debug_expire_wait(unsigned long long budget_ns, void* stream);
+
+/* Drops the host-side descriptor cache.  Safe to call at any time when no
+ * other thread is inside the library. */
+void attn_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXATTN_H_ */

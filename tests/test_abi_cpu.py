@@ -1,0 +1,127 @@
+"""The C-ABI library on a host without a GPU: it builds, loads, exports every
+function include/exattn.h declares, and rejects bad arguments on the host
+before any CUDA call (so none of these calls touches a device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "exattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_40_gb300 import build
+    build.build()
+    from exact_attention_40_gb300 import exattn
+    return exattn
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_decode_paged", "attn_decode_workspace_bytes",
+                     "attn_get_device_status", "attn_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(so, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["EXATTN_OK", "EXATTN_ERR_INVALID_ARG", "EXATTN_ERR_UNSUPPORTED",
+                                 "EXATTN_ERR_ALIGNMENT", "EXATTN_ERR_WORKSPACE", "EXATTN_ERR_CUDA",
+                                 "EXATTN_ERR_TIMEOUT", "EXATTN_ERR_DEVICE_BOUNDS"]):
+        assert lib.attn_status_string(code) == name
+    assert lib.attn_status_string(99) == "EXATTN_UNKNOWN_STATUS"
+
+
+def test_workspace_arithmetic(lib):
+    split = lib.attn_decode_split_tokens()
+    assert split == 512 and split % 16 == 0
+    # 64 seqs, 32 heads, d=128, up to 512 blocks (8192 tokens) -> 16 splits
+    n = lib.attn_decode_workspace_bytes(64, 32, 128, 512, 16)
+    rows = 64 * 32 * 16
+    assert n == rows * 128 * 4 + ((rows * 4 + 15) // 16) * 16
+    assert lib.attn_decode_workspace_bytes(1, 1, 64, 1, 16) == 64 * 4 + 16
+    assert lib.attn_decode_workspace_bytes(1, 1, 96, 1, 16) == 0  # unsupported d
+    assert lib.attn_decode_workspace_bytes(1, 1, 128, 1, 32) == 0  # unsupported block size
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=128,
+        scale=0.1, causal=0):
+    return lib.lib.attn_fwd(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, None)
+
+
+def test_fwd_rejections(lib):
+    assert fwd(lib, d=96) == 2
+    assert fwd(lib, Hq=3, Hkv=2) == 1
+    assert fwd(lib, Hkv=0) == 1
+    assert fwd(lib, Nq=-1) == 1
+    assert fwd(lib, scale=0.0) == 1
+    assert fwd(lib, scale=float("nan")) == 1
+    assert fwd(lib, q=None) == 1
+    assert fwd(lib, out=FAKE + 8) == 3
+    assert fwd(lib, k=FAKE + 2) == 3
+    assert fwd(lib, lse=FAKE + 2) == 3
+    assert fwd(lib, Nq=(1 << 30) + 1) == 2
+    assert fwd(lib, B=70000) == 2
+    # empty problems are successful no-ops, even with null pointers
+    assert fwd(lib, B=0, q=None, out=None) == 0
+    assert fwd(lib, Nq=0, q=None, out=None) == 0
+
+
+def dec(lib, ws_bytes=None, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, cl=FAKE, out=FAKE, lse=None, S=2, Hq=8, Hkv=2,
+             d=128, bs=16, nb=10, mb=4, scale=0.1, ws=FAKE)
+    a.update(kw)
+    if ws_bytes is None:
+        ws_bytes = lib.attn_decode_workspace_bytes(a["S"], a["Hq"], a["d"], a["mb"], 16)
+    return lib.lib.attn_decode_paged(a["q"], a["kc"], a["vc"], a["bt"], a["cl"], a["out"], a["lse"],
+                                     a["S"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["nb"], a["mb"],
+                                     a["scale"], a["ws"], ws_bytes, None)
+
+
+def test_decode_rejections(lib):
+    assert dec(lib, bs=32) == 2
+    assert dec(lib, d=80) == 2
+    assert dec(lib, Hq=6, Hkv=4) == 1
+    assert dec(lib, mb=0) == 1
+    assert dec(lib, kc=None) == 1
+    assert dec(lib, bt=FAKE + 2) == 3
+    assert dec(lib, q=FAKE + 4) == 3
+    assert dec(lib, ws=None) == 4
+    assert dec(lib, ws_bytes=16) == 4
+    assert dec(lib, ws=FAKE + 4) == 3
+    assert dec(lib, S=0, q=None) == 0
+    assert dec(lib, S=70000) == 2
+
+
+def test_debug_wait_budget_validated(lib):
+    assert lib.lib.attn_debug_expire_wait(0, None) == 1
+    assert lib.lib.attn_debug_expire_wait(10 ** 11, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """The binding has no fallback: without libexattn.so, importing it raises."""
+    import importlib.util
+    src = os.path.join(ROOT, "exact_attention_40_gb300", "exattn.py")
+    dst = tmp_path / "exattn.py"
+    dst.write_text(open(src).read())
+    spec = importlib.util.spec_from_file_location("exattn_copy", str(dst))
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)
