@@ -192,28 +192,23 @@ def run_reference(args):
     return 0
 
 
-def cpu_baseline_leg():
-    """Oracle on this host's cores over a bounded sample (about 10-30 s)."""
+def cpu_baseline_leg(target_s=10.0):
+    """Oracle on this host's cores: whole passes of the prefill workload,
+    repeated until about target_s seconds of CPU work have run."""
     import oracle
     oracle.build()
     cfg = PREFILL_CFG
     q, k, v = synth.prefill_inputs(cfg)
-    rows = synth.sample_rows(cfg.seed + 100, cfg.B, cfg.Hq, cfg.N, 16)
+    passes, dt = 0, 0.0
     t0 = time.perf_counter()
-    oracle.attn_rows(q, k, v, rows, cfg.scale, cfg.causal)
-    dt = time.perf_counter() - t0
-    fl = prefill_row_flops(rows, cfg.N, cfg.N, cfg.d, cfg.causal)
-    # scale the sample so the leg takes roughly 10 s
-    reps = int(max(1, min(64, 10.0 / max(dt, 1e-3))))
-    rows = synth.sample_rows(cfg.seed + 100, cfg.B, cfg.Hq, cfg.N, min(cfg.N, 16 * reps))
-    t0 = time.perf_counter()
-    oracle.attn_rows(q, k, v, rows, cfg.scale, cfg.causal)
-    dt = time.perf_counter() - t0
-    fl = prefill_row_flops(rows, cfg.N, cfg.N, cfg.d, cfg.causal)
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": dt,
-            "sample": "%d seeded query rows (%d per head) of the llama3_8b_causal prefill, "
-                      "fp64, full score rows" % (len(rows), len(rows) // cfg.Hq)}
+    while dt < target_s and passes < 100:
+        oracle.attn(q, k, v, cfg.scale, cfg.causal)
+        passes += 1
+        dt = time.perf_counter() - t0
+    return {"value": passes * cfg.flops() / dt / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle", "seconds": dt,
+            "sample": "%d full pass(es) of the llama3_8b_causal prefill (all 65536 query rows), "
+                      "fp64, full score rows" % passes}
 
 
 def run_gpu(args):
