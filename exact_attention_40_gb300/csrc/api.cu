@@ -132,6 +132,11 @@ int decode_max_splits(int max_blocks_per_seq, int block_size) {
   return static_cast<int>((tokens + exattn::kDecodeSplitTokens - 1) / exattn::kDecodeSplitTokens);
 }
 
+// Split-KV scratch for attn_decode_paged_static, for callers that may not
+// allocate device memory.  One copy per GPU, alive until the process exits.
+__device__ __align__(256) unsigned char g_static_scratch[EXATTN_STATIC_SCRATCH_BYTES];
+void* g_static_scratch_ptr[kMaxDevices] = {};
+
 }  // namespace
 
 extern "C" {
@@ -271,6 +276,34 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
   if (exattn::launch_decode(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return EXATTN_ERR_CUDA;
   return EXATTN_OK;
+}
+
+int attn_decode_paged_static(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, const int32_t* ctx_lens, void* out,
+                             float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
+                             int num_blocks, int max_blocks_per_seq, float scale, void* stream) {
+  const size_t need = attn_decode_workspace_bytes(num_seqs, Hq, d, max_blocks_per_seq, block_size);
+  if (need > EXATTN_STATIC_SCRATCH_BYTES) return EXATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  {
+    // Once per device, with that device current: the host-side name of the
+    // array is not a device address, so look the address up and keep it.
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EXATTN_ERR_CUDA;
+    if (g_static_scratch_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+        return EXATTN_ERR_CUDA;
+      g_static_scratch_ptr[dev] = p;
+    }
+    scratch = g_static_scratch_ptr[dev];
+  }
+  // Same validation and kernels as the workspace entry point (need == 0
+  // means the arguments are invalid, and it reports which).
+  return attn_decode_paged(q, k_cache, v_cache, block_table, ctx_lens, out, lse, num_seqs, Hq, Hkv,
+                           d, block_size, num_blocks, max_blocks_per_seq, scale, scratch,
+                           EXATTN_STATIC_SCRATCH_BYTES, stream);
 }
 
 int attn_get_device_status(void* stream, unsigned int* status_out) {

@@ -38,6 +38,9 @@ lib.attn_decode_workspace_bytes.restype = _SZ
 lib.attn_decode_paged.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P,
                                   _SZ, _P]
 lib.attn_decode_paged.restype = _I
+lib.attn_decode_paged_static.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                         _F, _P]
+lib.attn_decode_paged_static.restype = _I
 lib.attn_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
 lib.attn_get_device_status.restype = _I
 lib.attn_status_string.argtypes = [_I]

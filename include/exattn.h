@@ -115,6 +115,43 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                       int max_blocks_per_seq, float scale, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/* Size of the static device scratch behind attn_decode_paged_static. */
+#define EXATTN_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * attn_decode_paged for callers that cannot allocate device memory.
+ * (The pages have no counterpart: this is a deployment convenience.)
+ *
+ * Some callers may not call cudaMalloc at all: a plugin hosted inside an
+ * inference server whose own pool owns every byte of device memory, or a
+ * latency-critical decode loop where cudaMalloc's implicit device-wide
+ * synchronisation is not allowed.  This entry point takes the same
+ * arguments as attn_decode_paged minus the workspace; its split-KV scratch
+ * is a file-scope static device array of EXATTN_STATIC_SCRATCH_BYTES (32 MiB)
+ * that every GPU which loads the library holds until the process exits.
+ * The caller still passes every input and output buffer.
+ *
+ * - Limit: when attn_decode_workspace_bytes(num_seqs, Hq, d,
+ *   max_blocks_per_seq, block_size) exceeds EXATTN_STATIC_SCRATCH_BYTES the
+ *   call returns EXATTN_ERR_WORKSPACE and launches nothing.  For example
+ *   64 sequences x 32 query heads at d = 128 with block tables of up to
+ *   8192 tokens need about 16 MiB and fit; use attn_decode_paged beyond
+ *   the limit.
+ * - No allocation: it calls no cudaMalloc/cudaFree or allocating library.
+ * - Set-up: the first call on a device, with that device current, looks up
+ *   the array's device address once (cudaGetSymbolAddress); make that first
+ *   call before any stream capture.
+ * - Sharing: every call on a device uses the same array, and the array
+ *   keeps the last call's contents.  Nothing in it needs to start at zero
+ *   (each split's partial result is written before it is read), but calls
+ *   whose executions overlap on the GPU (different streams, or several host
+ *   threads) race on it; serialise them on one stream.
+ */
+int attn_decode_paged_static(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, const int32_t* ctx_lens, void* out,
+                             float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
+                             int num_blocks, int max_blocks_per_seq, float scale, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the status word of the
  * current device: 0, or an OR of EXATTN_DEVICE_*_BIT.  Returns EXATTN_OK
