@@ -1,27 +1,34 @@
 // Prefill attention kernel for sm_103a.
 //
-// One CTA computes one 128-row query tile of one (batch, query head):
+// One CTA computes two consecutive 128-row query tiles (A, then B) of one
+// (batch, query head):
 //   O = softmax(scale * Q K^T + mask) V,  lse = log sum exp(scale * Q K^T)
-// streaming the keys/values of the mapped KV head in 128-row tiles, with
-// an online softmax so the score tile S and probability tile P exist only
-// in tensor memory / shared memory ("Fused Kernel Compiler" page,
-// subsection FlashAttention Integration, items 1-4).
+// streaming the keys/values of the mapped KV head in 128-row tiles, with an
+// online softmax, so the score tile S and the probability tile P exist only
+// in tensor memory ("Fused Kernel Compiler" page, subsection FlashAttention
+// Integration, items 1-4).  The two tiles share every K/V tile load.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax warpgroup: thread r owns query row r of the tile,
-//              which is TMEM lane r.  Reads S from TMEM, applies the mask,
-//              keeps the running max m and sum l, writes P (bf16) to shared
-//              memory, rescales O in TMEM when m grows by more than
-//              kRescaleThreshold (log2 units), and runs the epilogue.
-//   warp 4     TMA producer: Q once, then K_j / V_j tiles into two rings.
-//   warp 5     tcgen05 issuer (one thread): S_j = Q K_j^T into one of two
-//              TMEM S buffers, then O += P_{j-1} V_{j-1}; also owns the TMEM
-//              allocation.
+// Warp roles (320 threads):
+//   warps 0-3  softmax warpgroup of tile A; warps 4-7 that of tile B.  Thread
+//              r of a warpgroup owns query row r of its tile, which is TMEM
+//              lane r.  It reads S from TMEM, masks, keeps the running max m
+//              and sum l, writes P (bf16) back into TMEM over S, rescales O
+//              in TMEM when m grows by more than kRescaleThreshold (log2
+//              units), and runs the epilogue of its tile.
+//   warp 8     TMA producer: Q_A, Q_B once, then K_j, V_j into a 4-slot ring.
+//   warp 9     tcgen05 issuer (one thread), also owns the TMEM allocation.
+//              Issue order per key tile j:
+//                S_A = Q_A K_j^T,  O_B += P_B(j-1) V_(j-1),  S_B = Q_B K_j^T,
+//                O_A += P_A(j) V_j
+//              so the tensor core works on one tile while the other tile's
+//              softmax runs (the two warpgroups alternate).
 //
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+d).
-// Shared memory: every operand tile is stored as 128-row x 64-column bf16
-// sub-tiles (16 KB, 128-byte swizzle) exactly as TMA writes them; the MMA
-// descriptors read them in place (K-major for Q, K and P; MN-major for V).
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+d),
+// O_B [384,384+d).  P_X overwrites columns [0,64) of S_X as packed bf16
+// pairs and is the A operand of the P*V MMA straight from TMEM.
+// Shared memory: operand tiles are 128-row x 64-column bf16 sub-tiles
+// (16 KB, 128-byte swizzle) exactly as TMA writes them; the MMA descriptors
+// read them in place (K-major for Q and K, MN-major for V).
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -30,29 +37,25 @@
 namespace exattn {
 namespace {
 
-constexpr int kBM = 128;                  // query rows per tile (= TMEM lanes)
-constexpr int kBN = 128;                  // keys per tile
-constexpr int kThreads = 192;
-constexpr int kWarpLoad = 4;
-constexpr int kWarpMma = 5;
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
+constexpr int kBM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;  // keys per tile
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr int kRing = 4;  // K/V slots: K_j in slot 2j % 4, V_j in slot (2j+1) % 4
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;          // column of the O accumulator
-constexpr float kRescaleThreshold = 8.0f; // log2 units: p may reach 2^8 before O is rescaled
+__host__ __device__ constexpr uint32_t tmem_s_col(int x) { return x == 0 ? 0u : 128u; }
+__host__ __device__ constexpr uint32_t tmem_o_col(int x) { return x == 0 ? 256u : 384u; }
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p may reach 2^8 before O is rescaled
 constexpr uint32_t kSubTileBytes = 128 * 64 * 2;
 
 template <int D>
 struct alignas(1024) PrefillSmem {
-  uint8_t q[D / 64][kSubTileBytes];            // Q tile; reused as O staging
-  uint8_t k[kKStages][D / 64][kSubTileBytes];  // K ring
-  uint8_t v[kVStages][D / 64][kSubTileBytes];  // V ring
-  uint8_t p[kBN / 64][kSubTileBytes];          // P tile (bf16)
-  uint64_t q_full;
-  uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, mma_fin;
+  uint8_t q[2][D / 64][kSubTileBytes];        // Q_A, Q_B; each reused as O staging
+  uint8_t ring[kRing][D / 64][kSubTileBytes];  // K/V tiles
+  uint64_t q_full[2];
+  uint64_t full[kRing], empty[kRing];
+  uint64_t s_full[2], p_full[2][2], o_done[2], mma_fin;  // p_full[tile][64-key half]
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -61,7 +64,7 @@ struct KernelParams {
   float* lse;
   unsigned int* status;
   unsigned long long wait_ns;
-  int Hq, Hkv, Nq, Nk, group, n_qtiles, causal;
+  int Hq, Hkv, Nq, Nk, group, n_ctiles, n_bh, causal;
   float scale_log2;  // scale * log2(e)
 };
 
@@ -83,8 +86,76 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ void named_bar_softmax() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+__device__ __forceinline__ void named_bar_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+// O (+)= P V with P (bf16, 128 x kBN) read from TMEM.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Exponentials, packed-bf16 P and the partial row sum of one 64-key half
+// (keys 64*H ..) of the score row held in sr[]; P goes to TMEM columns
+// [32*H, 32*H + 32) of S.
+template <int H>
+__device__ __forceinline__ float softmax_exp_half(const uint32_t (&sr)[128], uint32_t t_s,
+                                                  float scale_log2, float m_use) {
+  const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+  const uint64_t nm2 = f2_pack(-m_use, -m_use);
+  uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int h = 2 * H; h < 2 * H + 2; ++h) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int pair = 16 * h + c;
+      const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * pair]), __uint_as_float(sr[2 * pair + 1])),
+                                 c2, nm2);
+      float x0, x1;
+      f2_unpack(x2, x0, x1);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
+      pk[c] = pack_bf16x2(p0, p1);
+    }
+    tmem_st_32x32b_x16(t_s + 16 * h, pk);
+  }
+  const uint64_t t2 = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
+  float s0, s1;
+  f2_unpack(t2, s0, s1);
+  return s0 + s1;
+}
+
+struct TileInfo {
+  int n_kv;    // key tiles this query tile needs
+  int n_full;  // leading key tiles that need no mask
+};
+
+__device__ __forceinline__ TileInfo tile_info(int row0, const KernelParams& p) {
+  TileInfo t;
+  if (row0 >= p.Nq) {
+    t.n_kv = 0;
+    t.n_full = 0;
+    return t;
+  }
+  const long long shift = static_cast<long long>(p.Nk) - p.Nq;  // bottom-right alignment
+  t.n_kv = (p.Nk + kBN - 1) / kBN;
+  t.n_full = p.Nk / kBN;
+  if (p.causal) {
+    const long long last = static_cast<long long>(row0) + kBM - 1 + shift;  // last key, last row
+    t.n_kv = min(t.n_kv, last < 0 ? 0 : static_cast<int>(last / kBN) + 1);
+    const long long first = static_cast<long long>(row0) + shift + 1;  // keys visible to row0
+    t.n_full = min(t.n_full, first <= 0 ? 0 : static_cast<int>(first / kBN));
+  }
+  t.n_full = min(t.n_full, t.n_kv);
+  return t;
 }
 
 template <int D>
@@ -99,48 +170,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: late (heavier under the causal mask) query tiles launch first.
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);
-  const int hq = blockIdx.y;
-  const int b = blockIdx.z;
+  // Work item from a 1-D grid ordered heaviest first across all heads: the
+  // slowest-varying index walks the query-row blocks from the last (the
+  // most keys under the causal mask) to the first.
+  const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_bh));
+  const int ct = p.n_ctiles - 1 - static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_bh));
+  const int hq = bh % p.Hq;
+  const int b = bh / p.Hq;
   const int hkv = hq / p.group;
-  const int m0 = qt * kBM;
+  const int m0 = ct * 2 * kBM;
   const int zq = b * p.Hq + hq;
   const int zk = b * p.Hkv + hkv;
-
-  // Key tiles this query tile needs, and how many of them need no mask.
-  const long long shift = static_cast<long long>(p.Nk) - p.Nq;  // bottom-right alignment
-  int n_kv = (p.Nk + kBN - 1) / kBN;
-  int n_full = p.Nk / kBN;
-  if (p.causal) {
-    const long long last = static_cast<long long>(m0) + kBM - 1 + shift;  // last key of last row
-    const int lim = last < 0 ? 0 : static_cast<int>(last / kBN) + 1;
-    n_kv = min(n_kv, lim);
-    const long long first = static_cast<long long>(m0) + shift + 1;  // keys visible to row m0
-    const int full_c = first <= 0 ? 0 : static_cast<int>(first / kBN);
-    n_full = min(n_full, full_c);
-  }
+  const TileInfo ti[2] = {tile_info(m0, p), tile_info(m0 + kBM, p)};
+  const int n_iter = max(ti[0].n_kv, ti[1].n_kv);
 
   if (warp == kWarpLoad && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
-    mbar_init(&sm.q_full, 1);
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sm.q_full[x], 1);
+      mbar_init(&sm.s_full[x], 1);
+      mbar_init(&sm.p_full[x][0], 128);
+      mbar_init(&sm.p_full[x][1], 128);
+      mbar_init(&sm.o_done[x], 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.s_free[s], 128);
-    }
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.o_done, 1);
     mbar_init(&sm.mma_fin, 1);
     sm.abort_flag = 0u;
     fence_mbar_init();
@@ -155,91 +214,174 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
-  int issued_k[kKStages] = {0, 0};
-  int issued_v[kVStages] = {0, 0};
-  bool issued_q = false;
+  int issued_use[kRing] = {0, 0, 0, 0};  // producer: loads issued per slot
+  bool issued_q[2] = {false, false};
   bool mma_issued = false;
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_kv > 0) {
+    if (lane == 0 && n_iter > 0) {
       const uint64_t keep = l2_policy_evict_last();  // K/V tiles are re-read by other CTAs
-      mbar_arrive_expect_tx(&sm.q_full, D * kBM * 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q[c], &tm_q, &sm.q_full, c * 64, m0, zq);
-      issued_q = true;
-      for (int j = 0; j < n_kv; ++j) {
-        const int sk = j % kKStages;
-        if (j >= kKStages && !wait_or_abort(&sm.k_empty[sk], ((j / kKStages) - 1) & 1, p, &sm.abort_flag))
-          break;
-        mbar_arrive_expect_tx(&sm.k_full[sk], D * kBN * 2);
+      for (int x = 0; x < 2; ++x) {
+        if (ti[x].n_kv == 0) continue;
+        mbar_arrive_expect_tx(&sm.q_full[x], D * kBM * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d_hint(sm.k[sk][c], &tm_k, &sm.k_full[sk], c * 64, j * kBN, zk, keep);
-        issued_k[sk] = j / kKStages + 1;
-        const int sv = j % kVStages;
-        if (j >= kVStages && !wait_or_abort(&sm.v_empty[sv], ((j / kVStages) - 1) & 1, p, &sm.abort_flag))
-          break;
-        mbar_arrive_expect_tx(&sm.v_full[sv], D * kBN * 2);
+          tma_load_3d(sm.q[x][c], &tm_q, &sm.q_full[x], c * 64, m0 + x * kBM, zq);
+        issued_q[x] = true;
+      }
+      bool ok = true;
+      for (int j = 0; ok && j < n_iter; ++j) {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d_hint(sm.v[sv][c], &tm_v, &sm.v_full[sv], c * 64, j * kBN, zk, keep);
-        issued_v[sv] = j / kVStages + 1;
+        for (int part = 0; part < 2; ++part) {  // 0: K_j, 1: V_j
+          const int idx = 2 * j + part;
+          const int slot = idx % kRing;
+          const int use = idx / kRing;
+          if (use > 0 && !wait_or_abort(&sm.empty[slot], (use - 1) & 1, p, &sm.abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.full[slot], D * kBN * 2);
+          const CUtensorMap* tm = part == 0 ? &tm_k : &tm_v;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_hint(sm.ring[slot][c], tm, &sm.full[slot], c * 64, j * kBN, zk, keep);
+          issued_use[slot] = use + 1;
+        }
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    if (lane == 0 && n_iter > 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
-      bool ok = wait_or_abort(&sm.q_full, 0, p, &sm.abort_flag);
-      tc_fence_after_sync();
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int sk = j % kKStages;
-          if (!wait_or_abort(&sm.k_full[sk], (j / kKStages) & 1, p, &sm.abort_flag)) break;
-          if (j >= 2 && !wait_or_abort(&sm.s_free[j & 1], ((j >> 1) - 1) & 1, p, &sm.abort_flag)) break;
+      // Descriptors are built once; a k-step, sub-tile or ring slot moves
+      // only the start-address field (units of 16 bytes, no carry: shared
+      // addresses stay below 2^18).
+      constexpr uint32_t kSlotUnits = (D / 64) * kSubTileBytes / 16;
+      const uint64_t dq0 = smem_desc(smem_u32(&sm.q[0][0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t dq1 = smem_desc(smem_u32(&sm.q[1][0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t dk = smem_desc(smem_u32(&sm.ring[0][0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t dv = smem_desc(smem_u32(&sm.ring[0][0][0]), kSubTileBytes, 1024, kSwizzle128B);
+      const int nA = ti[0].n_kv, nB = ti[1].n_kv;
+      bool q0_ready = false, q1_ready = false;
+      int v_waited = -1;  // highest j whose V_j full barrier has been observed
+      bool ok = true;
+
+      for (int j = 0; ok && j <= n_iter; ++j) {
+        // ---- S_A(j) = Q_A K_j^T
+        if (j < n_iter) {
+          const int kidx = 2 * j;
+          if (!wait_or_abort(&sm.full[kidx % kRing], (kidx / kRing) & 1, p, &sm.abort_flag)) break;
           tc_fence_after_sync();
-          const uint32_t d_s = tmem + static_cast<uint32_t>(j & 1) * kBN;
+          if (j < nA) {
+            if (!q0_ready) {
+              if (!wait_or_abort(&sm.q_full[0], 0, p, &sm.abort_flag)) break;
+              q0_ready = true;
+              tc_fence_after_sync();
+            }
+            const uint64_t kb = dk + static_cast<uint64_t>((kidx % kRing) * kSlotUnits);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = smem_desc(smem_u32(sm.q[kk / 4]) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(smem_u32(sm.k[sk][kk / 4]) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
-            umma_bf16_ss(d_s, a, bd, id_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
+              umma_bf16_ss(tmem + tmem_s_col(0), dq0 + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&sm.s_full[0]);
+            mma_issued = true;
           }
-          mma_issued = true;
-          umma_commit(&sm.s_full[j & 1]);
-          umma_commit(&sm.k_empty[sk]);
         }
+        // ---- O_B += P_B(j-1) V_(j-1), then V_(j-1) is free
         if (j >= 1) {
           const int jj = j - 1;
-          const int sv = jj % kVStages;
-          if (!wait_or_abort(&sm.v_full[sv], (jj / kVStages) & 1, p, &sm.abort_flag)) break;
-          if (!wait_or_abort(&sm.p_full, jj & 1, p, &sm.abort_flag)) break;
-          tc_fence_after_sync();
+          if (jj < nB) {
+            const int vidx = 2 * jj + 1;
+            if (jj > v_waited) {
+              if (!wait_or_abort(&sm.full[vidx % kRing], (vidx / kRing) & 1, p, &sm.abort_flag)) break;
+              v_waited = jj;
+            }
+            const uint64_t vb = dv + static_cast<uint64_t>((vidx % kRing) * kSlotUnits);
+            bool got = true;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t a = smem_desc(smem_u32(sm.p[kk / 4]) + (kk % 4) * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(smem_u32(sm.v[sv][0]) + kk * 2048, kSubTileBytes, 1024, kSwizzle128B);
-            umma_bf16_ss(tmem + kTmemO, a, bd, id_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int half = 0; half < 2; ++half) {
+              if (!wait_or_abort(&sm.p_full[1][half], jj & 1, p, &sm.abort_flag)) {
+                got = false;
+                break;
+              }
+              tc_fence_after_sync();
+#pragma unroll
+              for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+                umma_bf16_ts(tmem + tmem_o_col(1), tmem + tmem_s_col(1) + kk * 8, vb + kk * 128, id_pv,
+                             (jj > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (!got) break;
+            if (jj == nB - 1) umma_commit(&sm.o_done[1]);
+            mma_issued = true;
           }
-          mma_issued = true;
-          umma_commit(&sm.v_empty[sv]);
-          umma_commit(&sm.o_done);
+          umma_commit(&sm.empty[(2 * jj + 1) % kRing]);  // V_(j-1) no longer read
+        }
+        if (j < n_iter) {
+          const int kidx = 2 * j;
+          // ---- S_B(j) = Q_B K_j^T, then K_j is free
+          if (j < nB) {
+            if (!q1_ready) {
+              if (!wait_or_abort(&sm.q_full[1], 0, p, &sm.abort_flag)) break;
+              q1_ready = true;
+              tc_fence_after_sync();
+            }
+            const uint64_t kb = dk + static_cast<uint64_t>((kidx % kRing) * kSlotUnits);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
+              umma_bf16_ss(tmem + tmem_s_col(1), dq1 + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&sm.s_full[1]);
+            mma_issued = true;
+          }
+          umma_commit(&sm.empty[kidx % kRing]);  // K_j no longer read
+          // ---- O_A += P_A(j) V_j
+          if (j < nA) {
+            const int vidx = 2 * j + 1;
+            if (j > v_waited) {
+              if (!wait_or_abort(&sm.full[vidx % kRing], (vidx / kRing) & 1, p, &sm.abort_flag)) break;
+              v_waited = j;
+            }
+            const uint64_t vb = dv + static_cast<uint64_t>((vidx % kRing) * kSlotUnits);
+            bool got = true;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              if (!wait_or_abort(&sm.p_full[0][half], j & 1, p, &sm.abort_flag)) {
+                got = false;
+                break;
+              }
+              tc_fence_after_sync();
+#pragma unroll
+              for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+                umma_bf16_ts(tmem + tmem_o_col(0), tmem + tmem_s_col(0) + kk * 8, vb + kk * 128, id_pv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (!got) break;
+            if (j == nA - 1) umma_commit(&sm.o_done[0]);
+            mma_issued = true;
+          }
         }
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int r = warp * 32 + lane;  // row within the tile == TMEM lane
-    const int row = m0 + r;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const long long vis_last = static_cast<long long>(row) + shift;  // causal: keys <= vis_last
+    // ------------------------------------------------------------ softmax warpgroups
+    const int x = warp >> 2;                 // 0: tile A, 1: tile B
+    const int r = (warp & 3) * 32 + lane;    // row within the tile == TMEM lane
+    const int row = m0 + x * kBM + r;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t t_s = t_lane + tmem_s_col(x);
+    const uint32_t t_o = t_lane + tmem_o_col(x);
+    const int n_kv = x ? ti[1].n_kv : ti[0].n_kv;
+    const int n_full = x ? ti[1].n_full : ti[0].n_full;
+    const long long vis_last = static_cast<long long>(row) + p.Nk - p.Nq;  // causal: keys <= vis_last
     float m_ref = -INFINITY;  // reference max, log2 units
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      if (!__all_sync(0xffffffffu, wait_or_abort(&sm.s_full[j & 1], (j >> 1) & 1, p, &sm.abort_flag))) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(&sm.s_full[x], j & 1, p, &sm.abort_flag))) {
         ok = false;
         break;
       }
@@ -247,26 +389,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sr[kBN];
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(j & 1) * kBN + c * 32,
-                           *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_ld_32x32b_x32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_ld_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&sm.s_free[j & 1]);
 
-      float s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c]);
       if (j >= n_full) {
         const long long key0 = static_cast<long long>(j) * kBN;
         long long lim = static_cast<long long>(p.Nk) - key0;  // keys >= Nk do not exist
         if (p.causal) lim = min(lim, vis_last - key0 + 1);
+        const int lim32 = static_cast<int>(max(-1ll, min(lim, static_cast<long long>(kBN))));
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
-          if (c >= lim) s[c] = -INFINITY;
+          if (c >= lim32) sr[c] = 0xFF800000u;  // -inf
       }
-      float mx = s[0];
+      // Row maximum: four independent chains of three-input max.
+      float acc[4];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 4; ++k) acc[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 4]));
+#pragma unroll
+      for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          acc[k] = max3f(acc[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 4 + k]));
+      float mx = max3f(acc[0], acc[1], fmaxf(acc[2], acc[3]));
       mx *= p.scale_log2;
       float alpha = 1.f;
       bool rescale = false;
@@ -276,90 +420,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum = 0.f;
-      uint32_t pk[kBN / 2];
-#pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], p.scale_log2, -m_use));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.scale_log2, -m_use));
-        sum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + sum;
-
-      // P buffer and O are owned by the previous P*V until it completes.
-      if (j >= 1 && !__all_sync(0xffffffffu, wait_or_abort(&sm.o_done, (j - 1) & 1, p, &sm.abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      // tcgen05.ld/st are warp-collective: the whole warp rescales if any
-      // of its rows needs it (alpha is 1 for the others).
-      if (__any_sync(0xffffffffu, rescale) && j >= 1) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(t_lane + kTmemO + c * 32, o);
+      // p = 2^(s * scale * log2e - m); P row -> TMEM columns [0, 64) of S_X
+      // (two bf16 per 32-bit column), 32 keys at a time: column 16h gets
+      // keys 32h.., whose own S columns were already read.  Each 64-key half
+      // is handed to the MMA warp as soon as it is stored, so P*V on the
+      // first half overlaps the exponentials of the second.
+      float sum = softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use);
+      // Lazy rescale of O_X, placed after the first half so that half's
+      // score registers are free.  O_X is complete up to key tile j-1 here:
+      // P*V_(j-1) was issued before S_X(j), and s_full fires only after
+      // every earlier MMA has finished; the first P*V of tile j waits for
+      // the half-0 hand-off below.  tcgen05.ld/st are warp-collective: the
+      // whole warp rescales if any of its rows needs it (alpha is 1 for the
+      // others).
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld_32x32b_x16(t_o + c * 16, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_32x32b_x32(t_lane + kTmemO + c * 32, o);
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_32x32b_x16(t_o + c * 16, o);
         }
-        tmem_st_wait();
       }
-      // P row r -> two K-major swizzled sub-tiles (16-byte chunk c of a
-      // 128-byte row lands at chunk c ^ (row & 7)).
-#pragma unroll
-      for (int ch = 0; ch < kBN / 8; ++ch) {
-        const uint32_t base = smem_u32(sm.p[ch / 8]) + r * 128;
-        const uint32_t addr = base + (((ch % 8) ^ (r & 7)) << 4);
-        st_shared_v4(addr, pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-      }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&sm.p_full);
+      mbar_arrive(&sm.p_full[x][0]);
+      sum += softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use);
+      l = l * alpha + sum;
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&sm.p_full[x][1]);
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && n_kv > 0)
-      ok = __all_sync(0xffffffffu, wait_or_abort(&sm.o_done, (n_kv - 1) & 1, p, &sm.abort_flag));
-    tc_fence_after_sync();
-    const bool have = ok && n_kv > 0;  // warp-uniform
-    const bool row_has_keys = have && l > 0.f;
-    const float inv_l = row_has_keys ? 1.f / l : 0.f;
-    if (p.lse != nullptr && row < p.Nq) {
-      const float lse = row_has_keys ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-      p.lse[static_cast<size_t>(zq) * p.Nq + row] = lse;
-    }
-    // O row -> bf16 -> swizzled staging in the (now idle) Q buffer.
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      if (have) {
-        tmem_ld_32x32b_x32(t_lane + kTmemO + c * 32, o);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
+    if (row - r < p.Nq) {  // this tile has at least one real row
+      if (ok && n_kv > 0)
+        ok = __all_sync(0xffffffffu, wait_or_abort(&sm.o_done[x], 0, p, &sm.abort_flag));
+      tc_fence_after_sync();
+      const bool have = ok && n_kv > 0;  // warp-uniform
+      const bool row_has_keys = have && l > 0.f;
+      const float inv_l = row_has_keys ? 1.f / l : 0.f;
+      if (p.lse != nullptr && row < p.Nq) {
+        const float lse = row_has_keys ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        p.lse[static_cast<size_t>(zq) * p.Nq + row] = lse;
       }
-      uint32_t w[16];
+      // O row -> bf16 -> swizzled staging in this tile's (now idle) Q buffer.
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-      const uint32_t base = smem_u32(sm.q[c / 2]) + r * 128;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (have) {
+          tmem_ld_32x32b_x32(t_o + c * 32, o);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int ch = (c % 2) * 4 + i;
-        st_shared_v4(base + ((ch ^ (r & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+        const uint32_t base = smem_u32(sm.q[x][c / 2]) + r * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ch = (c % 2) * 4 + i;
+          st_shared_v4(base + ((ch ^ (r & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
       }
-    }
-    fence_proxy_async_smem();
-    named_bar_softmax();
-    if (r == 0) {
+      fence_proxy_async_smem();
+      named_bar_sync(1 + x);
+      if (r == 0) {
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_store_3d(&tm_o, sm.q[c], c * 64, m0, zq);
-      bulk_commit_group();
-      bulk_wait_group_read0();
+        for (int c = 0; c < D / 64; ++c) tma_store_3d(&tm_o, sm.q[x][c], c * 64, m0 + x * kBM, zq);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
     }
   }
 
@@ -370,11 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (aborted) {
     // Drain what is still in flight before the CTA's memory goes away.
     if (warp == kWarpLoad && lane == 0) {
-      if (issued_q) mbar_wait(&sm.q_full, 0, p.wait_ns);
-      for (int s = 0; s < kKStages; ++s)
-        if (issued_k[s] > 0) mbar_wait(&sm.k_full[s], (issued_k[s] - 1) & 1, p.wait_ns);
-      for (int s = 0; s < kVStages; ++s)
-        if (issued_v[s] > 0) mbar_wait(&sm.v_full[s], (issued_v[s] - 1) & 1, p.wait_ns);
+      for (int x = 0; x < 2; ++x)
+        if (issued_q[x]) mbar_wait(&sm.q_full[x], 0, p.wait_ns);
+      for (int s = 0; s < kRing; ++s)
+        if (issued_use[s] > 0) mbar_wait(&sm.full[s], (issued_use[s] - 1) & 1, p.wait_ns);
     }
     if (warp == kWarpMma && lane == 0 && mma_issued) {
       umma_commit(&sm.mma_fin);
@@ -408,14 +543,17 @@ cudaError_t launch_d(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t st
   kp.Nq = a.Nq;
   kp.Nk = a.Nk;
   kp.group = a.Hq / a.Hkv;
-  kp.n_qtiles = (a.Nq + kBM - 1) / kBM;
+  kp.n_ctiles = (a.Nq + 2 * kBM - 1) / (2 * kBM);
+  kp.n_bh = a.B * a.Hq;
   kp.causal = a.causal;
   kp.scale_log2 = a.scale * 1.4426950408889634f;
   const size_t smem = smem_bytes_for<D>();
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(kp.n_qtiles, a.Hq, a.B);
+  const long long n_cta = static_cast<long long>(kp.n_ctiles) * kp.n_bh;
+  if (n_cta > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+  dim3 grid(static_cast<unsigned>(n_cta));
   prefill_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, kp);
   return cudaGetLastError();
 }
