@@ -33,15 +33,17 @@ struct MapKey {
   int d;
   long long rows;
   long long planes;
+  int box_rows;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && d == o.d && rows == o.rows && planes == o.planes;
+    return ptr == o.ptr && d == o.d && rows == o.rows && planes == o.planes &&
+           box_rows == o.box_rows;
   }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
     h ^= (static_cast<uint64_t>(k.d) << 1) + static_cast<uint64_t>(k.rows) * 0xBF58476D1CE4E5B9ull;
-    h ^= static_cast<uint64_t>(k.planes) * 0x94D049BB133111EBull;
+    h ^= static_cast<uint64_t>(k.planes) * 0x94D049BB133111EBull + static_cast<uint64_t>(k.box_rows);
     return static_cast<size_t>(h ^ (h >> 31));
   }
 };
@@ -83,11 +85,12 @@ int device_state(int* dev, unsigned int** status) {
 }
 
 // Descriptor of a bf16 tensor viewed as [planes, rows, d] (d innermost),
-// loaded/stored in boxes of 128 rows x 64 columns with 128-byte swizzle;
-// rows past `rows` read as zero and are not written.  Caller holds g_mu.
+// loaded/stored in boxes of box_rows rows x 64 columns with 128-byte
+// swizzle; rows past `rows` read as zero and are not written.  Caller holds
+// g_mu.
 int tensor_map(int dev, const void* ptr, int d, long long rows, long long planes,
-               const CUtensorMap** out) {
-  const MapKey key{reinterpret_cast<uintptr_t>(ptr), d, rows, planes};
+               const CUtensorMap** out, int box_rows = 128) {
+  const MapKey key{reinterpret_cast<uintptr_t>(ptr), d, rows, planes, box_rows};
   auto& cache = g_maps[dev];
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -99,7 +102,7 @@ int tensor_map(int dev, const void* ptr, int d, long long rows, long long planes
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(planes)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t elem[3] = {1, 1, 1};
   CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
                         strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -225,14 +228,15 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                       int num_seqs, int Hq, int Hkv, int d, int block_size, int num_blocks,
                       int max_blocks_per_seq, float scale, void* workspace, size_t workspace_bytes,
                       void* stream) {
-  if (num_seqs < 0 || Hq < 1 || Hkv < 1 || num_blocks < 0 || max_blocks_per_seq < 1)
+  if (num_seqs < 0 || Hq < 1 || Hkv < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
     return EXATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !good_scale(scale)) return EXATTN_ERR_INVALID_ARG;
   if ((d != 64 && d != 128) || block_size != exattn::kDecodeBlockSize) return EXATTN_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
-  const long long ychunks = static_cast<long long>(Hkv) * ((group + 3) / 4);
+  const long long ychunks = static_cast<long long>(Hkv) * ((group + 15) / 16);
+  const long long cache_rows = static_cast<long long>(num_blocks) * Hkv * block_size;
   if (num_seqs > 65535 || Hq > 65535 || ychunks > 65535 ||
-      static_cast<long long>(max_blocks_per_seq) * block_size > (1 << 30))
+      static_cast<long long>(max_blocks_per_seq) * block_size > (1 << 30) || cache_rows > 0x7FFFFFFFll)
     return EXATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0) return EXATTN_OK;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
@@ -250,31 +254,37 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
-    const int rc = device_state(&dev, &g.status);
+    int rc = device_state(&dev, &g.status);
     if (rc != EXATTN_OK) return rc;
+    // Each (block, kv head) span is 16 rows of the cache viewed as
+    // [num_blocks * Hkv * 16, d]; one box = 16 rows x 64 columns.
+    if ((rc = tensor_map(dev, k_cache, d, cache_rows, 1, &a.tm_k, block_size)) != EXATTN_OK) return rc;
+    if ((rc = tensor_map(dev, v_cache, d, cache_rows, 1, &a.tm_v, block_size)) != EXATTN_OK) return rc;
+    g.wait_ns = wait_budget_ns();
+    const int splits = decode_max_splits(max_blocks_per_seq, block_size);
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.ctx_lens = ctx_lens;
+    a.out = out;
+    a.lse = lse;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        static_cast<size_t>(num_seqs) * Hq * splits * d * sizeof(float));
+    a.num_seqs = num_seqs;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.num_blocks = num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.max_splits = splits;
+    a.scale = scale;
+    // launched under the lock: the descriptors are copied into the kernel
+    // parameters at launch
+    if (exattn::launch_decode(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return EXATTN_ERR_CUDA;
   }
-  g.wait_ns = wait_budget_ns();
-  const int splits = decode_max_splits(max_blocks_per_seq, block_size);
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_table = block_table;
-  a.ctx_lens = ctx_lens;
-  a.out = out;
-  a.lse = lse;
-  a.ws_o = static_cast<float*>(workspace);
-  a.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                      static_cast<size_t>(num_seqs) * Hq * splits * d * sizeof(float));
-  a.num_seqs = num_seqs;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.d = d;
-  a.num_blocks = num_blocks;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.max_splits = splits;
-  a.scale = scale;
-  if (exattn::launch_decode(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return EXATTN_ERR_CUDA;
   return EXATTN_OK;
 }
 

@@ -5,18 +5,24 @@
 // sequence's logical blocks to physical ones ("Optimizing LLM Inference
 // ..." page, section Paged Attention and Dynamic KV Cache Management).  One
 // (block, kv head) of K (or V) is a contiguous 16 x d bf16 span (4 KB at
-// d = 128), fetched with one bulk copy.
+// d = 128).
 //
-// decode_split_kernel: one CTA per (sequence, kv head, group of 4 query
-//   heads, split of kDecodeSplitTokens tokens).  Each of its 4 warps owns
-//   every 4th block of the split, streams it through a private 3-stage
-//   shared-memory ring (cp.async.bulk + mbarrier), and keeps its own online
-//   softmax state (running max m, sum l, fp32 accumulator) for the 4 query
-//   heads.  At the end the 4 warp states merge in shared memory and the
-//   split writes its normalised partial output O_s and lse_s (natural log)
-//   to the caller's workspace.
-// decode_combine_kernel: one CTA per (sequence, query head): with
+// decode_split_kernel: one CTA per (sequence, kv head, group of up to 16
+//   query heads, split of kDecodeSplitTokens tokens).  Each of its warps
+//   owns every kWarps-th block of the split and streams it through a private
+//   shared-memory ring: TMA copies each span as 64-column x 16-row boxes with
+//   the 128-byte swizzle, so ldmatrix reads are bank-conflict free.  Per
+//   block the warp computes S = Q K^T (16 query heads x 16 tokens) and
+//   O += P V with mma.sync m16n8k16 (bf16 in, fp32 accumulate; the query
+//   heads of the GQA group are the 16 rows, padded with zeros), keeping an
+//   online softmax (running max m, sum l) on the accumulator fragments.  At
+//   the end the warps' states merge in shared memory and the split writes
+//   its normalised partial output O_s and lse_s (natural log) to the
+//   workspace.
+// decode_combine_kernel: one CTA per (sequence, query head):
 //   L = log sum_s exp(lse_s), o = sum_s exp(lse_s - L) O_s, lse = L.
+//   Launched with programmatic dependent launch so its launch overlaps the
+//   split kernel's tail.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -28,29 +34,27 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
-constexpr int kHeads = 4;  // query heads handled per CTA (GQA group chunk)
+constexpr int kRows = 16;  // query heads per CTA (mma M)
 constexpr int kBlk = kDecodeBlockSize;
 constexpr int kBlocksPerSplit = kDecodeSplitTokens / kBlk;
-constexpr int kMaxBlocksPerWarp = kBlocksPerSplit / kWarps;
-static_assert(kBlocksPerSplit % kWarps == 0, "split must divide among warps");
+constexpr int kMaxBlocksPerWarp = (kBlocksPerSplit + kWarps - 1) / kWarps;
 static_assert(kMaxBlocksPerWarp <= 32, "block ids are staged one per lane");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
+constexpr uint32_t kBoxBytes = kBlk * 64 * 2;  // 16 tokens x 64 columns, bf16
 
 template <int D>
-struct alignas(128) DecodeSmem {
-  static constexpr int kTileBytes = kBlk * D * 2;
-  uint8_t ring[kWarps][kStages][2][kTileBytes];  // [warp][stage][K|V]
-  float p[kWarps][kBlk][kHeads];                 // probabilities of the current block
-  float wm[kWarps][kHeads];                      // per-warp running max (log2 units)
-  float wl[kWarps][kHeads];                      // per-warp running sum
+struct alignas(1024) DecodeSmem {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;  // K boxes then V boxes
+  uint8_t ring[kWarps][kStages][kStageBytes];
+  float wm[kWarps][kRows];  // per-warp running max (log2 units)
+  float wl[kWarps][kRows];  // per-warp running sum
   uint64_t full[kWarps][kStages];
 };
 
 struct SplitParams {
   const __nv_bfloat16* q;
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
   const int32_t* block_table;
   const int32_t* ctx_lens;
   float* ws_o;
@@ -69,24 +73,53 @@ __device__ __forceinline__ int clamp_ctx(int n, int max_ctx, unsigned int* statu
   return n;
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared address of the 16-byte chunk holding (token, 8 columns starting at
+// col8 * 8) in a K or V tile stored as D/64 swizzled 16-row boxes.
+__device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int token, int col8) {
+  return base + (col8 >> 3) * kBoxBytes + token * 128 + (((col8 & 7) ^ (token & 7)) << 4);
+}
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitParams p) {
-  constexpr int kTileBytes = DecodeSmem<D>::kTileBytes;
-  constexpr int kLanesPerRow = D / 8;          // lanes covering one 16-byte-chunked token row
-  constexpr int kTokPerInstr = 32 / kLanesPerRow;
-  constexpr int kInstr = kBlk / kTokPerInstr;  // 16-byte loads per lane per K block
-  constexpr int kVals = kInstr * kHeads;       // partial dot products per lane
-  constexpr int kDimsPerLane = D / 32;         // P*V output columns owned per lane
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
+  constexpr int kKSteps = D / 16;   // QK^T k-steps
+  constexpr int kNTiles = D / 8;    // P V n-tiles
+  constexpr int kStageBytes = DecodeSmem<D>::kStageBytes;
+  constexpr int kBoxes = DecodeSmem<D>::kBoxes;
 
   extern __shared__ uint8_t smem_raw[];
   DecodeSmem<D>& sm = *reinterpret_cast<DecodeSmem<D>*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;  // mma group id: row g (and g + 8)
+  const int t = lane & 3;   // thread in group
   const int split = blockIdx.x;
   const int hkv = blockIdx.y / p.n_chunks;
   const int chunk = blockIdx.y % p.n_chunks;
@@ -101,10 +134,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitPa
   const int tok_end = min(ctx, tok0 + kDecodeSplitTokens);
   const int blk0 = tok0 / kBlk;
   const int n_blk = (tok_end - tok0 + kBlk - 1) / kBlk;
-  // this warp's blocks: blk0 + warp + kWarps * i
   const int my_n = n_blk > warp ? (n_blk - warp + kWarps - 1) / kWarps : 0;
 
-  // Physical block ids of this warp's blocks, one per lane.
+  // Physical block of this warp's i-th block, held by lane i.
   int phys_lane = -1;
   if (lane < my_n) {
     phys_lane = __ldg(p.block_table + static_cast<size_t>(seq) * p.max_blocks_per_seq + blk0 +
@@ -116,45 +148,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitPa
   }
 
   if (lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[warp][s], 1);
     fence_mbar_init();
   }
   __syncwarp();
 
-  const size_t head_stride = static_cast<size_t>(kTileBytes);                 // (block, head) span
-  const size_t block_stride = static_cast<size_t>(p.Hkv) * kTileBytes;      // one physical block
   const uint64_t stream_policy = l2_policy_evict_first();
-
-  // Query rows of the 4 heads, restricted to this lane's 8 dims, in fp32.
-  const int hq0 = hkv * p.group + chunk * kHeads;
-  const int dim0 = 8 * (lane % kLanesPerRow);
-  float qv[kHeads][8];
-#pragma unroll
-  for (int h = 0; h < kHeads; ++h) {
-    const bool valid = chunk * kHeads + h < p.group;
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (valid)
-      raw = *reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(seq) * p.Hq + hq0 + h) * D + dim0);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      qv[h][2 * e] = bf16lo(w[e]);
-      qv[h][2 * e + 1] = bf16hi(w[e]);
-    }
-  }
-
-  float m[kHeads], lpart[2], acc[kHeads][kDimsPerLane];
-#pragma unroll
-  for (int h = 0; h < kHeads; ++h) {
-    m[h] = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < kDimsPerLane; ++e) acc[h][e] = 0.f;
-  }
-  lpart[0] = lpart[1] = 0.f;
-
-  // Start the copy of this warp's i-th block into stage i % kStages (the
-  // whole warp calls this; lane 0 issues).  A skipped block (bad table
-  // entry) still completes its stage's phase so the ring stays in step.
+  // Start the copy of this warp's i-th block into stage i % kStages (whole
+  // warp calls; lane 0 issues).  A skipped block (bad table entry) still
+  // completes its stage's phase so the ring stays in step.
   auto issue = [&](int i) {
     const int ph = __shfl_sync(0xffffffffu, phys_lane, i);
     if (lane == 0) {
@@ -162,26 +166,56 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitPa
       if (ph < 0) {
         mbar_arrive(bar);
       } else {
-        const size_t off = static_cast<size_t>(ph) * block_stride + hkv * head_stride;
+        const int row = (ph * p.Hkv + hkv) * kBlk;
+        uint8_t* st = sm.ring[warp][i % kStages];
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-        bulk_load_hint(sm.ring[warp][i % kStages][0], p.k_cache + off, kTileBytes, bar, stream_policy);
-        bulk_load_hint(sm.ring[warp][i % kStages][1], p.v_cache + off, kTileBytes, bar, stream_policy);
+        mbar_arrive_expect_tx(bar, kStageBytes);
+#pragma unroll
+        for (int b = 0; b < kBoxes; ++b) {
+          tma_load_3d_hint(st + b * kBoxBytes, &tm_k, bar, b * 64, row, 0, stream_policy);
+          tma_load_3d_hint(st + (kBoxes + b) * kBoxBytes, &tm_v, bar, b * 64, row, 0, stream_policy);
+        }
       }
     }
   };
   int issued = 0;
   for (; issued < min(my_n, kStages); ++issued) issue(issued);
 
-  const int my_h0 = 2 * (lane & 1);  // heads whose scores this lane holds after the reduction
+  // Q as mma A fragments: row r = query head hq0 + r of this chunk (zero
+  // when r >= rows_here), k-step ks covers columns 16 ks .. 16 ks + 15.
+  const int hq0 = hkv * p.group + chunk * kRows;
+  const int rows_here = min(kRows, p.group - chunk * kRows);
+  uint32_t qa[kKSteps][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+    const size_t row_lo = (static_cast<size_t>(seq) * p.Hq + hq0 + g) * (D / 2);
+    const size_t row_hi = row_lo + 8 * (D / 2);
+#pragma unroll
+    for (int ks = 0; ks < kKSteps; ++ks) {
+      const int w = ks * 8 + t;  // 32-bit word of columns 16 ks + 2t, +1
+      qa[ks][0] = g < rows_here ? __ldg(q32 + row_lo + w) : 0u;
+      qa[ks][1] = g + 8 < rows_here ? __ldg(q32 + row_hi + w) : 0u;
+      qa[ks][2] = g < rows_here ? __ldg(q32 + row_lo + w + 4) : 0u;
+      qa[ks][3] = g + 8 < rows_here ? __ldg(q32 + row_hi + w + 4) : 0u;
+    }
+  }
+
+  float m[2] = {-INFINITY, -INFINITY};  // rows g, g + 8 (log2 units)
+  float l[2] = {0.f, 0.f};              // this thread's partial sums
+  float acc[kNTiles][4];
+#pragma unroll
+  for (int n = 0; n < kNTiles; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+  // ldmatrix lane roles: matrix mi = lane / 8, row ri = lane % 8.
+  const int mi = lane >> 3, ri = lane & 7;
+
   for (int i = 0; i < my_n; ++i) {
     const int st = i % kStages;
     const bool waited = mbar_wait(&sm.full[warp][st], (i / kStages) & 1, p.wait_ns);
     if (!__all_sync(0xffffffffu, waited)) {
       if (lane == 0) {
         atomicOr(p.status, 1u);  // EXATTN_DEVICE_TIMEOUT_BIT
-        // let copies still in flight land before the ring is reused
-        for (int j = i + 1; j < issued; ++j)
+        for (int j = i + 1; j < issued; ++j)  // let copies in flight land
           mbar_wait(&sm.full[warp][j % kStages], (j / kStages) & 1, p.wait_ns);
       }
       __syncwarp();
@@ -191,152 +225,118 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const SplitPa
     const int blk = blk0 + warp + kWarps * i;
     const int n_valid = min(kBlk, ctx - blk * kBlk);
     if (ph >= 0) {
-      const uint8_t* kt = sm.ring[warp][st][0];
-      const uint8_t* vt = sm.ring[warp][st][1];
-      // ---- scores: lane reads 16 bytes of token (kTokPerInstr*t + lane/kLanesPerRow)
-      float part[kVals];
+      const uint32_t kt = smem_u32(sm.ring[warp][st]);
+      const uint32_t vt = kt + kBoxes * kBoxBytes;
+      // ---- S = Q K^T: two n-tiles of 8 tokens
+      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int t = 0; t < kInstr; ++t) {
-        const uint4 kw = *reinterpret_cast<const uint4*>(kt + t * 512 + lane * 16);
-        const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
-        float kf[8];
+      for (int ks = 0; ks < kKSteps; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        // matrices: (tokens 0-7, cols lo), (0-7, hi), (8-15, lo), (8-15, hi)
+        ldsm_x4(tile_chunk(kt, ri + 8 * (mi >> 1), 2 * ks + (mi & 1)), b0, b1, b2, b3);
+        mma_bf16_16816(c[0], qa[ks], b0, b1);
+        mma_bf16_16816(c[1], qa[ks], b2, b3);
+      }
+      // ---- online softmax on the fragments: token of c[nt][e & 1] is
+      // 8 nt + 2t + (e & 1); e < 2 is row g, e >= 2 row g + 8.
+      float s[2][4];  // [row][nt * 2 + j]
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kf[2 * e] = bf16lo(w[e]);
-          kf[2 * e + 1] = bf16hi(w[e]);
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const bool ok = 8 * nt + 2 * t + jj < n_valid;
+          s[0][2 * nt + jj] = ok ? c[nt][jj] * p.scale_log2 : -INFINITY;
+          s[1][2 * nt + jj] = ok ? c[nt][2 + jj] * p.scale_log2 : -INFINITY;
         }
+      float alpha[2];
+      uint32_t pa[4];
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          float a = 0.f;
+      for (int r = 0; r < 2; ++r) {
+        float bm = max3f(s[r][0], s[r][1], fmaxf(s[r][2], s[r][3]));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        const float mn = fmaxf(m[r], bm);
+        alpha[r] = (mn == -INFINITY) ? 1.f : ex2_approx(m[r] - mn);
+        m[r] = mn;
+        float pr[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) a = fmaf(qv[h][e], kf[e], a);
-          part[t * kHeads + h] = a;
+        for (int e = 0; e < 4; ++e) pr[e] = (mn == -INFINITY) ? 0.f : ex2_approx(s[r][e] - mn);
+        l[r] = l[r] * alpha[r] + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+        pa[r] = pack_bf16x2(pr[0], pr[1]);      // a0 (row g) / a1 (row g + 8): tokens 2t, 2t+1
+        pa[2 + r] = pack_bf16x2(pr[2], pr[3]);  // a2 / a3: tokens 8 + 2t, 8 + 2t + 1
+      }
+#pragma unroll
+      for (int n = 0; n < kNTiles; ++n) {
+        acc[n][0] *= alpha[0];
+        acc[n][1] *= alpha[0];
+        acc[n][2] *= alpha[1];
+        acc[n][3] *= alpha[1];
+      }
+      // ---- O += P V; V rows of tokens >= n_valid are zeroed in the
+      // fragments (they may hold anything, NaN included).
+      const bool partial = n_valid < kBlk;
+      const uint32_t keep_b0 =
+          (2 * t < n_valid ? 0x0000FFFFu : 0u) | (2 * t + 1 < n_valid ? 0xFFFF0000u : 0u);
+      const uint32_t keep_b1 =
+          (2 * t + 8 < n_valid ? 0x0000FFFFu : 0u) | (2 * t + 9 < n_valid ? 0xFFFF0000u : 0u);
+#pragma unroll
+      for (int n = 0; n < kNTiles; n += 2) {
+        uint32_t b0, b1, b2, b3;
+        // matrices: (tokens 0-7, cols n), (8-15, n), (0-7, n+1), (8-15, n+1)
+        ldsm_x4_t(tile_chunk(vt, ri + 8 * (mi & 1), n + (mi >> 1)), b0, b1, b2, b3);
+        if (partial) {
+          b0 &= keep_b0;
+          b1 &= keep_b1;
+          b2 &= keep_b0;
+          b3 &= keep_b1;
         }
-      }
-      // ---- reduce-scatter across the kLanesPerRow lanes sharing a token:
-      // afterwards lane holds values 2*(lane % kLanesPerRow) + {0,1}.
-      int cnt = kVals;
-#pragma unroll
-      for (int mask = kLanesPerRow / 2; mask >= 1; mask >>= 1) {
-        const int half = cnt / 2;
-        const bool upper = (lane & mask) != 0;
-#pragma unroll
-        for (int k = 0; k < kVals / 2; ++k) {
-          if (k < half) {
-            const float send = upper ? part[k] : part[k + half];
-            const float keep = upper ? part[k + half] : part[k];
-            part[k] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-          }
-        }
-        cnt = half;
-      }
-      // value index v = 2*(lane % kLanesPerRow) + e  ->  instr t = v / 4, head v % 4
-      const int tok = kTokPerInstr * ((lane % kLanesPerRow) >> 1) + lane / kLanesPerRow;
-      float sc[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e)
-        sc[e] = (tok < n_valid) ? part[e] * p.scale_log2 : -INFINITY;
-      // ---- block max per head (lanes with equal lane&1 hold the same heads)
-      float bm[2] = {sc[0], sc[1]};
-#pragma unroll
-      for (int mask = 2; mask <= 16; mask <<= 1) {
-        bm[0] = fmaxf(bm[0], __shfl_xor_sync(0xffffffffu, bm[0], mask));
-        bm[1] = fmaxf(bm[1], __shfl_xor_sync(0xffffffffu, bm[1], mask));
-      }
-      const float om0 = __shfl_xor_sync(0xffffffffu, bm[0], 1);
-      const float om1 = __shfl_xor_sync(0xffffffffu, bm[1], 1);
-      const bool odd = (lane & 1) != 0;  // this lane holds heads 2,3 (else 0,1)
-      float blkmax[kHeads];
-      blkmax[0] = odd ? om0 : bm[0];
-      blkmax[1] = odd ? om1 : bm[1];
-      blkmax[2] = odd ? bm[0] : om0;
-      blkmax[3] = odd ? bm[1] : om1;
-      float alpha[kHeads];
-#pragma unroll
-      for (int h = 0; h < kHeads; ++h) {
-        const float mn = fmaxf(m[h], blkmax[h]);
-        alpha[h] = (mn == -INFINITY) ? 1.f : ex2_approx(m[h] - mn);
-        m[h] = mn;
-      }
-      float pv[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float mh = odd ? m[2 + e] : m[e];
-        const float ah = odd ? alpha[2 + e] : alpha[e];
-        pv[e] = (mh == -INFINITY) ? 0.f : ex2_approx(sc[e] - mh);
-        lpart[e] = lpart[e] * ah + pv[e];
-      }
-      *reinterpret_cast<float2*>(&sm.p[warp][tok][my_h0]) = make_float2(pv[0], pv[1]);
-      __syncwarp();
-      // ---- O += P V over the valid tokens; lane owns columns [kDimsPerLane*lane, +kDimsPerLane)
-#pragma unroll
-      for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-        for (int e = 0; e < kDimsPerLane; ++e) acc[h][e] *= alpha[h];
-      for (int t = 0; t < n_valid; ++t) {
-        const float4 pt = *reinterpret_cast<const float4*>(&sm.p[warp][t][0]);
-        float vf[kDimsPerLane];
-        if constexpr (kDimsPerLane == 4) {
-          const uint2 vw = *reinterpret_cast<const uint2*>(vt + t * (D * 2) + lane * 8);
-          vf[0] = bf16lo(vw.x);
-          vf[1] = bf16hi(vw.x);
-          vf[2] = bf16lo(vw.y);
-          vf[3] = bf16hi(vw.y);
-        } else {
-          const uint32_t vw = *reinterpret_cast<const uint32_t*>(vt + t * (D * 2) + lane * 4);
-          vf[0] = bf16lo(vw);
-          vf[1] = bf16hi(vw);
-        }
-        const float pp[kHeads] = {pt.x, pt.y, pt.z, pt.w};
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-          for (int e = 0; e < kDimsPerLane; ++e) acc[h][e] = fmaf(pp[h], vf[e], acc[h][e]);
+        mma_bf16_16816(acc[n], pa, b0, b1);
+        mma_bf16_16816(acc[n + 1], pa, b2, b3);
       }
     }
     __syncwarp();  // all lanes done with this stage before it is refilled
     if (issued < my_n) issue(issued++);
   }
 
-  // ---- per-warp totals of l for all 4 heads
+  // ---- per-warp totals of l (the four lanes of a row group)
 #pragma unroll
-  for (int mask = 2; mask <= 16; mask <<= 1) {
-    lpart[0] += __shfl_xor_sync(0xffffffffu, lpart[0], mask);
-    lpart[1] += __shfl_xor_sync(0xffffffffu, lpart[1], mask);
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
   }
-  if (lane < 2) {
-    sm.wm[warp][2 * lane] = m[2 * lane];
-    sm.wm[warp][2 * lane + 1] = m[2 * lane + 1];
-    sm.wl[warp][2 * lane] = lpart[0];
-    sm.wl[warp][2 * lane + 1] = lpart[1];
+  if (t == 0) {
+    sm.wm[warp][g] = m[0];
+    sm.wm[warp][g + 8] = m[1];
+    sm.wl[warp][g] = l[0];
+    sm.wl[warp][g + 8] = l[1];
   }
   __syncthreads();  // every warp finished streaming: the rings are free
-  float* wacc = reinterpret_cast<float*>(&sm.ring[0][0][0][0]);  // [warp][head][D]
+  float* wacc = reinterpret_cast<float*>(&sm.ring[0][0][0]);  // [warp][row][D]
 #pragma unroll
-  for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-    for (int e = 0; e < kDimsPerLane; ++e)
-      wacc[(warp * kHeads + h) * D + kDimsPerLane * lane + e] = acc[h][e];
+  for (int n = 0; n < kNTiles; ++n) {
+    const int col = 8 * n + 2 * t;
+    *reinterpret_cast<float2*>(&wacc[(warp * kRows + g) * D + col]) = make_float2(acc[n][0], acc[n][1]);
+    *reinterpret_cast<float2*>(&wacc[(warp * kRows + g + 8) * D + col]) =
+        make_float2(acc[n][2], acc[n][3]);
+  }
   __syncthreads();
 
-  // ---- merge the 4 warps; thread -> (head, column) pairs
-  for (int idx = threadIdx.x; idx < kHeads * D; idx += kThreads) {
-    const int h = idx / D, col = idx % D;
-    if (chunk * kHeads + h >= p.group) continue;
+  // ---- merge the warps; thread -> (row, column) pairs of real heads
+  for (int idx = threadIdx.x; idx < rows_here * D; idx += kThreads) {
+    const int r = idx / D, col = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][r]);
     float L = 0.f, o = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float wt = (sm.wm[w][h] == -INFINITY) ? 0.f : ex2_approx(sm.wm[w][h] - M);
-        L += wt * sm.wl[w][h];
-        o += wt * wacc[(w * kHeads + h) * D + col];
+        const float wt = (sm.wm[w][r] == -INFINITY) ? 0.f : ex2_approx(sm.wm[w][r] - M);
+        L += wt * sm.wl[w][r];
+        o += wt * wacc[(w * kRows + r) * D + col];
       }
     }
-    const int hq = hq0 + h;
-    const size_t slot = (static_cast<size_t>(seq) * p.Hq + hq) * p.max_splits + split;
+    const size_t slot = (static_cast<size_t>(seq) * p.Hq + hq0 + r) * p.max_splits + split;
     p.ws_o[slot * D + col] = (L > 0.f) ? o / L : 0.f;
     if (col == 0) p.ws_lse[slot] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
   }
@@ -354,6 +354,9 @@ struct CombineParams {
 
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineParams p) {
+  // Programmatic dependent launch: this grid may start before the split
+  // kernel has finished; wait for its results here.
+  cudaGridDependencySynchronize();
   const int hq = blockIdx.x;
   const int seq = blockIdx.y;
   const int col = threadIdx.x;
@@ -379,17 +382,15 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineParams p
 
 template <int D>
 size_t split_smem_bytes() {
-  return sizeof(DecodeSmem<D>) + 128;
+  return sizeof(DecodeSmem<D>) + 1024;
 }
 
 template <int D>
 cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t stream) {
-  static_assert(sizeof(float) * kWarps * kHeads * D <= sizeof(DecodeSmem<D>::ring),
+  static_assert(sizeof(float) * kWarps * kRows * D <= sizeof(DecodeSmem<D>::ring),
                 "merge scratch must fit in the rings");
   SplitParams sp;
   sp.q = static_cast<const __nv_bfloat16*>(a.q);
-  sp.k_cache = static_cast<const uint8_t*>(a.k_cache);
-  sp.v_cache = static_cast<const uint8_t*>(a.v_cache);
   sp.block_table = a.block_table;
   sp.ctx_lens = a.ctx_lens;
   sp.ws_o = a.ws_o;
@@ -399,7 +400,7 @@ cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t str
   sp.Hq = a.Hq;
   sp.Hkv = a.Hkv;
   sp.group = a.Hq / a.Hkv;
-  sp.n_chunks = (sp.group + kHeads - 1) / kHeads;
+  sp.n_chunks = (sp.group + kRows - 1) / kRows;
   sp.num_blocks = a.num_blocks;
   sp.max_blocks_per_seq = a.max_blocks_per_seq;
   sp.max_splits = a.max_splits;
@@ -410,7 +411,7 @@ cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t str
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_splits, a.Hkv * sp.n_chunks, a.num_seqs);
-  decode_split_kernel<D><<<grid, kThreads, smem, stream>>>(sp);
+  decode_split_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_k, *a.tm_v, sp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -424,8 +425,17 @@ cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t str
   cp.Hq = a.Hq;
   cp.max_blocks_per_seq = a.max_blocks_per_seq;
   cp.max_splits = a.max_splits;
-  decode_combine_kernel<D><<<dim3(a.Hq, a.num_seqs), D, 0, stream>>>(cp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hq, a.num_seqs);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, cp);
 }
 
 }  // namespace

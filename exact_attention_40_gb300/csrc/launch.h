@@ -32,6 +32,8 @@ constexpr int kDecodeSplitTokens = 512;
 constexpr int kDecodeBlockSize = 16;
 
 struct DecodeArgs {
+  const CUtensorMap* tm_k;  // cache viewed as [num_blocks * Hkv * 16 rows, d], 16-row boxes
+  const CUtensorMap* tm_v;
   const void* q;
   const void* k_cache;
   const void* v_cache;

@@ -105,7 +105,7 @@ size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_p
  * block_size must be 16.  The key/value sweep of each sequence is cut into
  * splits of split_tokens (512) tokens; each split yields a partial output
  * and log-sum-exp, and a second kernel merges them (exact up to rounding).
- * Two kernel launches.  A ctx_len of 0 gives o = 0, lse = -inf; a
+ * Two kernel launches.  num_blocks >= 1.  A ctx_len of 0 gives o = 0, lse = -inf; a
  * ctx_len above max_blocks_per_seq * block_size or a table entry outside
  * [0, num_blocks) is clamped/skipped and flagged in the device status word.
  */

@@ -100,6 +100,7 @@ def test_decode_rejections(lib):
     assert dec(lib, d=80) == 2
     assert dec(lib, Hq=6, Hkv=4) == 1
     assert dec(lib, mb=0) == 1
+    assert dec(lib, nb=0) == 1
     assert dec(lib, kc=None) == 1
     assert dec(lib, bt=FAKE + 2) == 3
     assert dec(lib, q=FAKE + 4) == 3
