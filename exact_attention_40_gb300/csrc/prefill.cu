@@ -43,6 +43,9 @@ constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr int kRing = 4;  // K/V slots: K_j in slot 2j % 4, V_j in slot (2j+1) % 4
+// Copies travel in pairs: pair j = {V_(j-1), K_j} shares one completion
+// barrier and one release (pair slot j % 2): K_j and V_(j-1) are both done
+// once S_B(j) is issued, since O_B += P_B(j-1) V_(j-1) precedes it.
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t tmem_s_col(int x) { return x == 0 ? 0u : 128u; }
 __host__ __device__ constexpr uint32_t tmem_o_col(int x) { return x == 0 ? 256u : 384u; }
@@ -54,8 +57,8 @@ struct alignas(1024) PrefillSmem {
   uint8_t q[2][D / 64][kSubTileBytes];        // Q_A, Q_B; each reused as O staging
   uint8_t ring[kRing][D / 64][kSubTileBytes];  // K/V tiles
   uint64_t q_full[2];
-  uint64_t full[kRing], empty[kRing];
-  uint64_t s_full[2], p_full[2][2], o_done[2], mma_fin;  // p_full[tile][64-key half]
+  uint64_t full[2], empty[2];  // per pair slot: pair j = {V_(j-1), K_j}
+  uint64_t s_full[2], p_full[2], o_done[2], mma_fin;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -192,11 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.q_full[x], 1);
       mbar_init(&sm.s_full[x], 1);
-      mbar_init(&sm.p_full[x][0], 128);
-      mbar_init(&sm.p_full[x][1], 128);
+      mbar_init(&sm.p_full[x], 128);
       mbar_init(&sm.o_done[x], 1);
     }
-    for (int s = 0; s < kRing; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
-  int issued_use[kRing] = {0, 0, 0, 0};  // producer: loads issued per slot
+  int issued_pairs[2] = {0, 0};  // producer: copy pairs issued per pair slot
   bool issued_q[2] = {false, false};
   bool mma_issued = false;
 
@@ -230,24 +232,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sm.q[x][c], &tm_q, &sm.q_full[x], c * 64, m0 + x * kBM, zq);
         issued_q[x] = true;
       }
-      bool ok = true;
-      for (int j = 0; ok && j < n_iter; ++j) {
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {  // 0: K_j, 1: V_j
-          const int idx = 2 * j + part;
-          const int slot = idx % kRing;
-          const int use = idx / kRing;
-          if (use > 0 && !wait_or_abort(&sm.empty[slot], (use - 1) & 1, p, &sm.abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.full[slot], D * kBN * 2);
-          const CUtensorMap* tm = part == 0 ? &tm_k : &tm_v;
+      for (int pp = 0; pp <= n_iter; ++pp) {  // pair pp = {V_(pp-1), K_pp}
+        const int ps = pp & 1;
+        if (pp >= 2 && !wait_or_abort(&sm.empty[ps], ((pp >> 1) - 1) & 1, p, &sm.abort_flag)) break;
+        const bool has_v = pp >= 1, has_k = pp < n_iter;
+        mbar_arrive_expect_tx(&sm.full[ps], (has_v + has_k) * D * kBN * 2);
+        if (has_v) {
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d_hint(sm.ring[slot][c], tm, &sm.full[slot], c * 64, j * kBN, zk, keep);
-          issued_use[slot] = use + 1;
+            tma_load_3d_hint(sm.ring[(2 * pp - 1) % kRing][c], &tm_v, &sm.full[ps], c * 64,
+                             (pp - 1) * kBN, zk, keep);
         }
+        if (has_k) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_hint(sm.ring[(2 * pp) % kRing][c], &tm_k, &sm.full[ps], c * 64, pp * kBN, zk,
+                             keep);
+        }
+        issued_pairs[ps] = (pp >> 1) + 1;
       }
     }
   } else if (warp == kWarpMma) {
@@ -265,104 +267,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv = smem_desc(smem_u32(&sm.ring[0][0][0]), kSubTileBytes, 1024, kSwizzle128B);
       const int nA = ti[0].n_kv, nB = ti[1].n_kv;
       bool q0_ready = false, q1_ready = false;
-      int v_waited = -1;  // highest j whose V_j full barrier has been observed
-      bool ok = true;
 
+      auto qk = [&](int x, uint64_t dq, int j) {
+        const uint64_t kb = dk + static_cast<uint64_t>(((2 * j) % kRing) * kSlotUnits);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
+          umma_bf16_ss(tmem + tmem_s_col(x), dq + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&sm.s_full[x]);
+      };
+      auto pv = [&](int x, int j) {
+        const uint64_t vb = dv + static_cast<uint64_t>(((2 * j + 1) % kRing) * kSlotUnits);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_bf16_ts(tmem + tmem_o_col(x), tmem + tmem_s_col(x) + kk * 8, vb + kk * 128, id_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+      };
+
+      // pair 0 = {K_0}
+      bool ok = wait_or_abort(&sm.full[0], 0, p, &sm.abort_flag);
+      tc_fence_after_sync();
       for (int j = 0; ok && j <= n_iter; ++j) {
-        // ---- S_A(j) = Q_A K_j^T
-        if (j < n_iter) {
-          const int kidx = 2 * j;
-          if (!wait_or_abort(&sm.full[kidx % kRing], (kidx / kRing) & 1, p, &sm.abort_flag)) break;
+        // ---- S_A(j) = Q_A K_j^T   (K_j arrived with pair j, awaited below
+        // in iteration j-1, or above for j = 0)
+        if (j < nA) {
+          if (!q0_ready) {
+            if (!wait_or_abort(&sm.q_full[0], 0, p, &sm.abort_flag)) break;
+            q0_ready = true;
+            tc_fence_after_sync();
+          }
+          qk(0, dq0, j);
+          mma_issued = true;
+        }
+        // ---- O_B += P_B(j-1) V_(j-1)
+        if (j >= 1 && j - 1 < nB) {
+          if (!wait_or_abort(&sm.p_full[1], (j - 1) & 1, p, &sm.abort_flag)) break;
           tc_fence_after_sync();
-          if (j < nA) {
-            if (!q0_ready) {
-              if (!wait_or_abort(&sm.q_full[0], 0, p, &sm.abort_flag)) break;
-              q0_ready = true;
-              tc_fence_after_sync();
-            }
-            const uint64_t kb = dk + static_cast<uint64_t>((kidx % kRing) * kSlotUnits);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
-              umma_bf16_ss(tmem + tmem_s_col(0), dq0 + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&sm.s_full[0]);
-            mma_issued = true;
-          }
+          pv(1, j - 1);
+          if (j - 1 == nB - 1) umma_commit(&sm.o_done[1]);
+          mma_issued = true;
         }
-        // ---- O_B += P_B(j-1) V_(j-1), then V_(j-1) is free
-        if (j >= 1) {
-          const int jj = j - 1;
-          if (jj < nB) {
-            const int vidx = 2 * jj + 1;
-            if (jj > v_waited) {
-              if (!wait_or_abort(&sm.full[vidx % kRing], (vidx / kRing) & 1, p, &sm.abort_flag)) break;
-              v_waited = jj;
-            }
-            const uint64_t vb = dv + static_cast<uint64_t>((vidx % kRing) * kSlotUnits);
-            bool got = true;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              if (!wait_or_abort(&sm.p_full[1][half], jj & 1, p, &sm.abort_flag)) {
-                got = false;
-                break;
-              }
-              tc_fence_after_sync();
-#pragma unroll
-              for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
-                umma_bf16_ts(tmem + tmem_o_col(1), tmem + tmem_s_col(1) + kk * 8, vb + kk * 128, id_pv,
-                             (jj > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (!got) break;
-            if (jj == nB - 1) umma_commit(&sm.o_done[1]);
-            mma_issued = true;
+        if (j == n_iter) break;
+        // ---- S_B(j) = Q_B K_j^T
+        if (j < nB) {
+          if (!q1_ready) {
+            if (!wait_or_abort(&sm.q_full[1], 0, p, &sm.abort_flag)) break;
+            q1_ready = true;
+            tc_fence_after_sync();
           }
-          umma_commit(&sm.empty[(2 * jj + 1) % kRing]);  // V_(j-1) no longer read
+          qk(1, dq1, j);
+          mma_issued = true;
         }
-        if (j < n_iter) {
-          const int kidx = 2 * j;
-          // ---- S_B(j) = Q_B K_j^T, then K_j is free
-          if (j < nB) {
-            if (!q1_ready) {
-              if (!wait_or_abort(&sm.q_full[1], 0, p, &sm.abort_flag)) break;
-              q1_ready = true;
-              tc_fence_after_sync();
-            }
-            const uint64_t kb = dk + static_cast<uint64_t>((kidx % kRing) * kSlotUnits);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
-              umma_bf16_ss(tmem + tmem_s_col(1), dq1 + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&sm.s_full[1]);
-            mma_issued = true;
-          }
-          umma_commit(&sm.empty[kidx % kRing]);  // K_j no longer read
-          // ---- O_A += P_A(j) V_j
-          if (j < nA) {
-            const int vidx = 2 * j + 1;
-            if (j > v_waited) {
-              if (!wait_or_abort(&sm.full[vidx % kRing], (vidx / kRing) & 1, p, &sm.abort_flag)) break;
-              v_waited = j;
-            }
-            const uint64_t vb = dv + static_cast<uint64_t>((vidx % kRing) * kSlotUnits);
-            bool got = true;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              if (!wait_or_abort(&sm.p_full[0][half], j & 1, p, &sm.abort_flag)) {
-                got = false;
-                break;
-              }
-              tc_fence_after_sync();
-#pragma unroll
-              for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
-                umma_bf16_ts(tmem + tmem_o_col(0), tmem + tmem_s_col(0) + kk * 8, vb + kk * 128, id_pv,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (!got) break;
-            if (j == nA - 1) umma_commit(&sm.o_done[0]);
-            mma_issued = true;
-          }
+        umma_commit(&sm.empty[j & 1]);  // pair j = {V_(j-1), K_j} no longer read
+        // ---- pair j+1 = {V_j, K_(j+1)}, then O_A += P_A(j) V_j
+        if (!wait_or_abort(&sm.full[(j + 1) & 1], ((j + 1) >> 1) & 1, p, &sm.abort_flag)) break;
+        tc_fence_after_sync();
+        if (j < nA) {
+          if (!wait_or_abort(&sm.p_full[0], j & 1, p, &sm.abort_flag)) break;
+          tc_fence_after_sync();
+          pv(0, j);
+          if (j == nA - 1) umma_commit(&sm.o_done[0]);
+          mma_issued = true;
         }
       }
     }
@@ -422,15 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       // p = 2^(s * scale * log2e - m); P row -> TMEM columns [0, 64) of S_X
       // (two bf16 per 32-bit column), 32 keys at a time: column 16h gets
-      // keys 32h.., whose own S columns were already read.  Each 64-key half
-      // is handed to the MMA warp as soon as it is stored, so P*V on the
-      // first half overlaps the exponentials of the second.
+      // keys 32h.., whose own S columns were already read.  The whole row
+      // is handed over at once (two 4-MMA halves with a wait between them
+      // measured slower than one 8-MMA group).
       float sum = softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use);
       // Lazy rescale of O_X, placed after the first half so that half's
       // score registers are free.  O_X is complete up to key tile j-1 here:
       // P*V_(j-1) was issued before S_X(j), and s_full fires only after
-      // every earlier MMA has finished; the first P*V of tile j waits for
-      // the half-0 hand-off below.  tcgen05.ld/st are warp-collective: the
+      // every earlier MMA has finished; P*V of tile j waits for the hand-off
+      // below.  tcgen05.ld/st are warp-collective: the
       // whole warp rescales if any of its rows needs it (alpha is 1 for the
       // others).
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
@@ -444,14 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_32x32b_x16(t_o + c * 16, o);
         }
       }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&sm.p_full[x][0]);
       sum += softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use);
       l = l * alpha + sum;
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&sm.p_full[x][1]);
+      mbar_arrive(&sm.p_full[x]);
     }
 
     // ------------------------------------------------------------ epilogue
@@ -508,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpLoad && lane == 0) {
       for (int x = 0; x < 2; ++x)
         if (issued_q[x]) mbar_wait(&sm.q_full[x], 0, p.wait_ns);
-      for (int s = 0; s < kRing; ++s)
-        if (issued_use[s] > 0) mbar_wait(&sm.full[s], (issued_use[s] - 1) & 1, p.wait_ns);
+      for (int s = 0; s < 2; ++s)
+        if (issued_pairs[s] > 0) mbar_wait(&sm.full[s], (issued_pairs[s] - 1) & 1, p.wait_ns);
     }
     if (warp == kWarpMma && lane == 0 && mma_issued) {
       umma_commit(&sm.mma_fin);
