@@ -184,7 +184,6 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
     if (rc != EXATTN_OK) return rc;
     const long long pq = static_cast<long long>(B) * Hq, pk = static_cast<long long>(B) * Hkv;
     if ((rc = tensor_map(dev, q, d, Nq, pq, &a.tm_q)) != EXATTN_OK) return rc;
-    if ((rc = tensor_map(dev, out, d, Nq, pq, &a.tm_o)) != EXATTN_OK) return rc;
     if (Nk > 0) {
       if ((rc = tensor_map(dev, k, d, Nk, pk, &a.tm_k)) != EXATTN_OK) return rc;
       if ((rc = tensor_map(dev, v, d, Nk, pk, &a.tm_v)) != EXATTN_OK) return rc;
@@ -193,6 +192,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
       a.tm_v = a.tm_q;
     }
     g.wait_ns = wait_budget_ns();
+    a.out = out;
     a.lse = lse;
     a.B = B;
     a.Hq = Hq;

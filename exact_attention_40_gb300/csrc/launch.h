@@ -18,7 +18,7 @@ struct PrefillArgs {
   const CUtensorMap* tm_q;
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
-  const CUtensorMap* tm_o;
+  void* out;  // [B, Hq, Nq, d] bf16, written with plain 16-byte stores
   float* lse;
   int B, Hq, Hkv, Nq, Nk, d;
   int causal;

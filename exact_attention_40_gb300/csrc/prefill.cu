@@ -1,12 +1,18 @@
 // Prefill attention kernel for sm_103a.
 //
-// One CTA computes two consecutive 128-row query tiles (A, then B) of one
-// (batch, query head):
+// Computes, for every (batch, query head) and query row,
 //   O = softmax(scale * Q K^T + mask) V,  lse = log sum exp(scale * Q K^T)
 // streaming the keys/values of the mapped KV head in 128-row tiles, with an
 // online softmax, so the score tile S and the probability tile P exist only
 // in tensor memory ("Fused Kernel Compiler" page, subsection FlashAttention
-// Integration, items 1-4).  The two tiles share every K/V tile load.
+// Integration, items 1-4).
+//
+// Persistent: one CTA per SM walks a static list of work items; an item is
+// two consecutive 128-row query tiles (A, B) of one (batch, query head) that
+// share every K/V tile load.  Items are numbered heaviest first and dealt in
+// a snake order so heavy and light items pair up under the causal mask; the
+// next item's Q copy and first S = Q K^T overlap the previous item's
+// epilogue.
 //
 // Warp roles (320 threads):
 //   warps 0-3  softmax warpgroup of tile A; warps 4-7 that of tile B.  Thread
@@ -14,8 +20,9 @@
 //              lane r.  It reads S from TMEM, masks, keeps the running max m
 //              and sum l, writes P (bf16) back into TMEM over S, rescales O
 //              in TMEM when m grows by more than kRescaleThreshold (log2
-//              units), and runs the epilogue of its tile.
-//   warp 8     TMA producer: Q_A, Q_B once, then K_j, V_j into a 4-slot ring.
+//              units), and writes its O row and lse in the epilogue.
+//   warp 8     TMA producer: Q_A, Q_B per item, then K/V copies in pairs
+//              {V_(j-1), K_j} through a 4-slot ring.
 //   warp 9     tcgen05 issuer (one thread), also owns the TMEM allocation.
 //              Issue order per key tile j:
 //                S_A = Q_A K_j^T,  O_B += P_B(j-1) V_(j-1),  S_B = Q_B K_j^T,
@@ -28,7 +35,8 @@
 // pairs and is the A operand of the P*V MMA straight from TMEM.
 // Shared memory: operand tiles are 128-row x 64-column bf16 sub-tiles
 // (16 KB, 128-byte swizzle) exactly as TMA writes them; the MMA descriptors
-// read them in place (K-major for Q and K, MN-major for V).
+// read them in place (K-major for Q and K, MN-major for V).  Every barrier
+// phase is derived from running counters that carry across items.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -56,7 +64,7 @@ template <int D>
 struct alignas(1024) PrefillSmem {
   uint8_t q[2][D / 64][kSubTileBytes];        // Q_A, Q_B; each reused as O staging
   uint8_t ring[kRing][D / 64][kSubTileBytes];  // K/V tiles
-  uint64_t q_full[2];
+  uint64_t q_full[2], q_free[2];  // Q tile landed / Q buffer no longer read
   uint64_t full[2], empty[2];  // per pair slot: pair j = {V_(j-1), K_j}
   uint64_t s_full[2], p_full[2], o_done[2], mma_fin;
   uint32_t tmem_base;
@@ -64,10 +72,11 @@ struct alignas(1024) PrefillSmem {
 };
 
 struct KernelParams {
+  __nv_bfloat16* out;
   float* lse;
   unsigned int* status;
   unsigned long long wait_ns;
-  int Hq, Hkv, Nq, Nk, group, n_ctiles, n_bh, causal;
+  int Hq, Hkv, Nq, Nk, group, n_ctiles, n_bh, n_items, causal;
   float scale_log2;  // scale * log2(e)
 };
 
@@ -87,10 +96,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
       return false;
     }
   }
-}
-
-__device__ __forceinline__ void named_bar_sync(int id) {
-  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
 // O (+)= P V with P (bf16, 128 x kBN) read from TMEM.
@@ -161,11 +166,41 @@ __device__ __forceinline__ TileInfo tile_info(int row0, const KernelParams& p) {
   return t;
 }
 
+// One work item = two consecutive 128-row query tiles of one (batch, query
+// head).  Items are numbered heaviest first (the query blocks with the most
+// keys under the causal mask first, across all heads).
+struct Item {
+  int zq, zk, m0, n_iter;
+  TileInfo ti[2];
+};
+
+__device__ __forceinline__ Item item_at(int idx, const KernelParams& p) {
+  Item it;
+  const int bh = idx % p.n_bh;
+  const int ct = p.n_ctiles - 1 - idx / p.n_bh;
+  const int hq = bh % p.Hq;
+  const int b = bh / p.Hq;
+  it.zq = b * p.Hq + hq;
+  it.zk = b * p.Hkv + hq / p.group;
+  it.m0 = ct * 2 * kBM;
+  it.ti[0] = tile_info(it.m0, p);
+  it.ti[1] = tile_info(it.m0 + kBM, p);
+  it.n_iter = max(it.ti[0].n_kv, it.ti[1].n_kv);
+  return it;
+}
+
+// Persistent schedule: CTA c takes, in round r, item r * G + c (r even) or
+// r * G + G - 1 - c (r odd), G = gridDim.x.  With heaviest-first numbering
+// this pairs heavy with light items.
+__device__ __forceinline__ int item_index(int round) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return round * G + ((round & 1) ? (G - 1 - c) : c);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const KernelParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem<D>& sm = *reinterpret_cast<PrefillSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -173,27 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item from a 1-D grid ordered heaviest first across all heads: the
-  // slowest-varying index walks the query-row blocks from the last (the
-  // most keys under the causal mask) to the first.
-  const int bh = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_bh));
-  const int ct = p.n_ctiles - 1 - static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_bh));
-  const int hq = bh % p.Hq;
-  const int b = bh / p.Hq;
-  const int hkv = hq / p.group;
-  const int m0 = ct * 2 * kBM;
-  const int zq = b * p.Hq + hq;
-  const int zk = b * p.Hkv + hkv;
-  const TileInfo ti[2] = {tile_info(m0, p), tile_info(m0 + kBM, p)};
-  const int n_iter = max(ti[0].n_kv, ti[1].n_kv);
-
   if (warp == kWarpLoad && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.q_full[x], 1);
+      mbar_init(&sm.q_free[x], 1);
       mbar_init(&sm.s_full[x], 1);
       mbar_init(&sm.p_full[x], 128);
       mbar_init(&sm.o_done[x], 1);
@@ -217,223 +238,269 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   int issued_pairs[2] = {0, 0};  // producer: copy pairs issued per pair slot
-  bool issued_q[2] = {false, false};
+  int q_loads[2] = {0, 0};       // producer: Q tiles issued per buffer
   bool mma_issued = false;
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_iter > 0) {
+    if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();  // K/V tiles are re-read by other CTAs
-      for (int x = 0; x < 2; ++x) {
-        if (ti[x].n_kv == 0) continue;
-        mbar_arrive_expect_tx(&sm.q_full[x], D * kBM * 2);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm.q[x][c], &tm_q, &sm.q_full[x], c * 64, m0 + x * kBM, zq);
-        issued_q[x] = true;
-      }
-      for (int pp = 0; pp <= n_iter; ++pp) {  // pair pp = {V_(pp-1), K_pp}
-        const int ps = pp & 1;
-        if (pp >= 2 && !wait_or_abort(&sm.empty[ps], ((pp >> 1) - 1) & 1, p, &sm.abort_flag)) break;
-        const bool has_v = pp >= 1, has_k = pp < n_iter;
-        mbar_arrive_expect_tx(&sm.full[ps], (has_v + has_k) * D * kBN * 2);
-        if (has_v) {
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d_hint(sm.ring[(2 * pp - 1) % kRing][c], &tm_v, &sm.full[ps], c * 64,
-                             (pp - 1) * kBN, zk, keep);
-        }
-        if (has_k) {
+      int g = 0;  // running pair index: pair g uses slot g & 1
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int idx = item_index(round);
+        if (idx >= p.n_items) break;
+        const Item it = item_at(idx, p);
+        if (it.n_iter == 0) continue;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (it.ti[x].n_kv == 0) continue;
+          // the previous Q of this buffer must have been read by its last S
+          if (q_loads[x] > 0 && !wait_or_abort(&sm.q_free[x], (q_loads[x] - 1) & 1, p, &sm.abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.q_full[x], D * kBM * 2);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d_hint(sm.ring[(2 * pp) % kRing][c], &tm_k, &sm.full[ps], c * 64, pp * kBN, zk,
-                             keep);
+            tma_load_3d(sm.q[x][c], &tm_q, &sm.q_full[x], c * 64, it.m0 + x * kBM, it.zq);
+          ++q_loads[x];
         }
-        issued_pairs[ps] = (pp >> 1) + 1;
+        for (int pp = 0; ok && pp <= it.n_iter; ++pp, ++g) {  // pair pp = {V_(pp-1), K_pp}
+          const int ps = g & 1;
+          if (g >= 2 && !wait_or_abort(&sm.empty[ps], ((g >> 1) - 1) & 1, p, &sm.abort_flag)) {
+            ok = false;
+            break;
+          }
+          const bool has_v = pp >= 1, has_k = pp < it.n_iter;
+          mbar_arrive_expect_tx(&sm.full[ps], (has_v + has_k) * D * kBN * 2);
+          if (has_v) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d_hint(sm.ring[(2 * g + 3) % kRing][c], &tm_v, &sm.full[ps], c * 64,
+                               (pp - 1) * kBN, it.zk, keep);
+          }
+          if (has_k) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d_hint(sm.ring[(2 * g) % kRing][c], &tm_k, &sm.full[ps], c * 64, pp * kBN,
+                               it.zk, keep);
+          }
+          issued_pairs[ps] = (g >> 1) + 1;
+        }
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_iter > 0) {
+    if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
       // Descriptors are built once; a k-step, sub-tile or ring slot moves
       // only the start-address field (units of 16 bytes, no carry: shared
       // addresses stay below 2^18).
       constexpr uint32_t kSlotUnits = (D / 64) * kSubTileBytes / 16;
-      const uint64_t dq0 = smem_desc(smem_u32(&sm.q[0][0][0]), 16, 1024, kSwizzle128B);
-      const uint64_t dq1 = smem_desc(smem_u32(&sm.q[1][0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t dq[2] = {smem_desc(smem_u32(&sm.q[0][0][0]), 16, 1024, kSwizzle128B),
+                              smem_desc(smem_u32(&sm.q[1][0][0]), 16, 1024, kSwizzle128B)};
       const uint64_t dk = smem_desc(smem_u32(&sm.ring[0][0][0]), 16, 1024, kSwizzle128B);
       const uint64_t dv = smem_desc(smem_u32(&sm.ring[0][0][0]), kSubTileBytes, 1024, kSwizzle128B);
-      const int nA = ti[0].n_kv, nB = ti[1].n_kv;
-      bool q0_ready = false, q1_ready = false;
+      int g = 0;                  // running pair index (as the producer's)
+      int q_waits[2] = {0, 0};    // completions of q_full[x] consumed
+      int p_waits[2] = {0, 0};    // completions of p_full[x] consumed
 
-      auto qk = [&](int x, uint64_t dq, int j) {
-        const uint64_t kb = dk + static_cast<uint64_t>(((2 * j) % kRing) * kSlotUnits);
+      // S_X = Q_X K^T with K in the ring slot of running pair gk
+      auto qk = [&](int x, int gk) {
+        const uint64_t kb = dk + static_cast<uint64_t>(((2 * gk) % kRing) * kSlotUnits);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
-          umma_bf16_ss(tmem + tmem_s_col(x), dq + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + tmem_s_col(x), dq[x] + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&sm.s_full[x]);
       };
-      auto pv = [&](int x, int j) {
-        const uint64_t vb = dv + static_cast<uint64_t>(((2 * j + 1) % kRing) * kSlotUnits);
+      // O_X (+)= P_X V with V in the ring slot of running pair gv
+      auto pv = [&](int x, int gv, bool first) {
+        const uint64_t vb = dv + static_cast<uint64_t>(((2 * gv + 3) % kRing) * kSlotUnits);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           umma_bf16_ts(tmem + tmem_o_col(x), tmem + tmem_s_col(x) + kk * 8, vb + kk * 128, id_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+                       (!first || kk > 0) ? 1u : 0u);
+      };
+      auto wait_p = [&](int x) -> bool {
+        if (!wait_or_abort(&sm.p_full[x], p_waits[x] & 1, p, &sm.abort_flag)) return false;
+        ++p_waits[x];
+        tc_fence_after_sync();
+        return true;
+      };
+      auto wait_q = [&](int x) -> bool {
+        if (!wait_or_abort(&sm.q_full[x], q_waits[x] & 1, p, &sm.abort_flag)) return false;
+        ++q_waits[x];
+        tc_fence_after_sync();
+        return true;
       };
 
-      // pair 0 = {K_0}
-      bool ok = wait_or_abort(&sm.full[0], 0, p, &sm.abort_flag);
-      tc_fence_after_sync();
-      for (int j = 0; ok && j <= n_iter; ++j) {
-        // ---- S_A(j) = Q_A K_j^T   (K_j arrived with pair j, awaited below
-        // in iteration j-1, or above for j = 0)
-        if (j < nA) {
-          if (!q0_ready) {
-            if (!wait_or_abort(&sm.q_full[0], 0, p, &sm.abort_flag)) break;
-            q0_ready = true;
-            tc_fence_after_sync();
-          }
-          qk(0, dq0, j);
-          mma_issued = true;
-        }
-        // ---- O_B += P_B(j-1) V_(j-1)
-        if (j >= 1 && j - 1 < nB) {
-          if (!wait_or_abort(&sm.p_full[1], (j - 1) & 1, p, &sm.abort_flag)) break;
-          tc_fence_after_sync();
-          pv(1, j - 1);
-          if (j - 1 == nB - 1) umma_commit(&sm.o_done[1]);
-          mma_issued = true;
-        }
-        if (j == n_iter) break;
-        // ---- S_B(j) = Q_B K_j^T
-        if (j < nB) {
-          if (!q1_ready) {
-            if (!wait_or_abort(&sm.q_full[1], 0, p, &sm.abort_flag)) break;
-            q1_ready = true;
-            tc_fence_after_sync();
-          }
-          qk(1, dq1, j);
-          mma_issued = true;
-        }
-        umma_commit(&sm.empty[j & 1]);  // pair j = {V_(j-1), K_j} no longer read
-        // ---- pair j+1 = {V_j, K_(j+1)}, then O_A += P_A(j) V_j
-        if (!wait_or_abort(&sm.full[(j + 1) & 1], ((j + 1) >> 1) & 1, p, &sm.abort_flag)) break;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int idx = item_index(round);
+        if (idx >= p.n_items) break;
+        const Item it = item_at(idx, p);
+        if (it.n_iter == 0) continue;
+        const int nA = it.ti[0].n_kv, nB = it.ti[1].n_kv, n_iter = it.n_iter;
+        const int base = g;  // running index of this item's pair 0 = {K_0}
+        if (!wait_or_abort(&sm.full[base & 1], (base >> 1) & 1, p, &sm.abort_flag)) break;
         tc_fence_after_sync();
-        if (j < nA) {
-          if (!wait_or_abort(&sm.p_full[0], j & 1, p, &sm.abort_flag)) break;
+        for (int j = 0; j <= n_iter; ++j) {
+          // ---- S_A(j) = Q_A K_j^T   (K_j came with pair base + j)
+          if (j < nA) {
+            if (j == 0 && !(ok = wait_q(0))) break;
+            qk(0, base + j);
+            if (j == nA - 1) umma_commit(&sm.q_free[0]);  // Q_A no longer read
+            mma_issued = true;
+          }
+          // ---- O_B += P_B(j-1) V_(j-1)
+          if (j >= 1 && j - 1 < nB) {
+            if (!(ok = wait_p(1))) break;
+            pv(1, base + j, j == 1);
+            if (j - 1 == nB - 1) umma_commit(&sm.o_done[1]);
+            mma_issued = true;
+          }
+          if (j == n_iter) {
+            umma_commit(&sm.empty[(base + j) & 1]);  // last pair {V_(n-1)} no longer read
+            break;
+          }
+          // ---- S_B(j) = Q_B K_j^T
+          if (j < nB) {
+            if (j == 0 && !(ok = wait_q(1))) break;
+            qk(1, base + j);
+            if (j == nB - 1) umma_commit(&sm.q_free[1]);
+            mma_issued = true;
+          }
+          umma_commit(&sm.empty[(base + j) & 1]);  // pair {V_(j-1), K_j} no longer read
+          // ---- pair base+j+1 = {V_j, K_(j+1)}, then O_A += P_A(j) V_j
+          const int gn = base + j + 1;
+          if (!(ok = wait_or_abort(&sm.full[gn & 1], (gn >> 1) & 1, p, &sm.abort_flag))) break;
           tc_fence_after_sync();
-          pv(0, j);
-          if (j == nA - 1) umma_commit(&sm.o_done[0]);
-          mma_issued = true;
+          if (j < nA) {
+            if (!(ok = wait_p(0))) break;
+            pv(0, gn, j == 0);
+            if (j == nA - 1) umma_commit(&sm.o_done[0]);
+            mma_issued = true;
+          }
         }
+        g = base + n_iter + 1;
       }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int x = warp >> 2;                 // 0: tile A, 1: tile B
     const int r = (warp & 3) * 32 + lane;    // row within the tile == TMEM lane
-    const int row = m0 + x * kBM + r;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t t_s = t_lane + tmem_s_col(x);
     const uint32_t t_o = t_lane + tmem_o_col(x);
-    const int n_kv = x ? ti[1].n_kv : ti[0].n_kv;
-    const int n_full = x ? ti[1].n_full : ti[0].n_full;
-    const long long vis_last = static_cast<long long>(row) + p.Nk - p.Nq;  // causal: keys <= vis_last
-    float m_ref = -INFINITY;  // reference max, log2 units
-    float l = 0.f;
+    int s_waits = 0, o_waits = 0;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!__all_sync(0xffffffffu, wait_or_abort(&sm.s_full[x], j & 1, p, &sm.abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      uint32_t sr[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld_32x32b_x32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tmem_ld_wait();
-
-      if (j >= n_full) {
-        const long long key0 = static_cast<long long>(j) * kBN;
-        long long lim = static_cast<long long>(p.Nk) - key0;  // keys >= Nk do not exist
-        if (p.causal) lim = min(lim, vis_last - key0 + 1);
-        const int lim32 = static_cast<int>(max(-1ll, min(lim, static_cast<long long>(kBN))));
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= lim32) sr[c] = 0xFF800000u;  // -inf
-      }
-      // Row maximum: four independent chains of three-input max.
-      float acc[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 4]));
-#pragma unroll
-      for (int c = 8; c < kBN; c += 8)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          acc[k] = max3f(acc[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 4 + k]));
-      float mx = max3f(acc[0], acc[1], fmaxf(acc[2], acc[3]));
-      mx *= p.scale_log2;
-      float alpha = 1.f;
-      bool rescale = false;
-      if (mx > m_ref + kRescaleThreshold) {
-        alpha = ex2_approx(m_ref - mx);  // 0 when m_ref is -inf
-        m_ref = mx;
-        rescale = true;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // p = 2^(s * scale * log2e - m); P row -> TMEM columns [0, 64) of S_X
-      // (two bf16 per 32-bit column), 32 keys at a time: column 16h gets
-      // keys 32h.., whose own S columns were already read.  The whole row
-      // is handed over at once (two 4-MMA halves with a wait between them
-      // measured slower than one 8-MMA group).
-      float sum = softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use);
-      // Lazy rescale of O_X, placed after the first half so that half's
-      // score registers are free.  O_X is complete up to key tile j-1 here:
-      // P*V_(j-1) was issued before S_X(j), and s_full fires only after
-      // every earlier MMA has finished; P*V of tile j waits for the hand-off
-      // below.  tcgen05.ld/st are warp-collective: the
-      // whole warp rescales if any of its rows needs it (alpha is 1 for the
-      // others).
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld_32x32b_x16(t_o + c * 16, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_32x32b_x16(t_o + c * 16, o);
+    for (int round = 0; ok; ++round) {
+      const int idx = item_index(round);
+      if (idx >= p.n_items) break;
+      const Item it = item_at(idx, p);
+      const int row0 = it.m0 + x * kBM;
+      if (row0 >= p.Nq) continue;  // this tile does not exist
+      const int row = row0 + r;
+      const int n_kv = it.ti[x].n_kv;
+      const int n_full = it.ti[x].n_full;
+      const long long vis_last = static_cast<long long>(row) + p.Nk - p.Nq;  // causal: keys <= vis_last
+      float m_ref = -INFINITY;  // reference max, log2 units
+      float l = 0.f;
+      for (int j = 0; j < n_kv; ++j) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&sm.s_full[x], s_waits & 1, p, &sm.abort_flag))) {
+          ok = false;
+          break;
         }
-      }
-      sum += softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use);
-      l = l * alpha + sum;
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(&sm.p_full[x]);
-    }
+        ++s_waits;
+        tc_fence_after_sync();
+        uint32_t sr[kBN];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld_32x32b_x32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_ld_wait();
 
-    // ------------------------------------------------------------ epilogue
-    if (row - r < p.Nq) {  // this tile has at least one real row
-      if (ok && n_kv > 0)
-        ok = __all_sync(0xffffffffu, wait_or_abort(&sm.o_done[x], 0, p, &sm.abort_flag));
-      tc_fence_after_sync();
-      const bool have = ok && n_kv > 0;  // warp-uniform
-      const bool row_has_keys = have && l > 0.f;
+        if (j >= n_full) {
+          const long long key0 = static_cast<long long>(j) * kBN;
+          long long lim = static_cast<long long>(p.Nk) - key0;  // keys >= Nk do not exist
+          if (p.causal) lim = min(lim, vis_last - key0 + 1);
+          const int lim32 = static_cast<int>(max(-1ll, min(lim, static_cast<long long>(kBN))));
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= lim32) sr[c] = 0xFF800000u;  // -inf
+        }
+        // Row maximum: four independent chains of three-input max.
+        float acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 4]));
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            acc[k] = max3f(acc[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 4 + k]));
+        float mx = max3f(acc[0], acc[1], fmaxf(acc[2], acc[3]));
+        mx *= p.scale_log2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_ref + kRescaleThreshold) {
+          alpha = ex2_approx(m_ref - mx);  // 0 when m_ref is -inf
+          m_ref = mx;
+          rescale = true;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // p = 2^(s * scale * log2e - m); P row -> TMEM columns [0, 64) of
+        // S_X (two bf16 per 32-bit column), 32 keys at a time: column 16h
+        // gets keys 32h.., whose own S columns were already read.  The whole
+        // row is handed over at once (two 4-MMA halves with a wait between
+        // them measured slower than one 8-MMA group).
+        float sum = softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use);
+        // Lazy rescale of O_X, placed after the first half so that half's
+        // score registers are free.  O_X is complete up to key tile j-1
+        // here: P*V_(j-1) was issued before S_X(j), and s_full fires only
+        // after every earlier MMA has finished; P*V of tile j waits for the
+        // hand-off below.  tcgen05.ld/st are warp-collective: the whole warp
+        // rescales if any of its rows needs it (alpha is 1 for the others).
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld_32x32b_x16(t_o + c * 16, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_32x32b_x16(t_o + c * 16, o);
+          }
+        }
+        sum += softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use);
+        l = l * alpha + sum;
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&sm.p_full[x]);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      // O row -> 1/l -> bf16 -> straight to global memory (16-byte stores;
+      // rows past Nq are skipped), so the Q buffer is free for the next
+      // item as soon as its last S has been computed.
+      if (n_kv > 0) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&sm.o_done[x], o_waits & 1, p, &sm.abort_flag))) break;
+        ++o_waits;
+        tc_fence_after_sync();
+      }
+      const bool row_has_keys = n_kv > 0 && l > 0.f;
       const float inv_l = row_has_keys ? 1.f / l : 0.f;
       if (p.lse != nullptr && row < p.Nq) {
         const float lse = row_has_keys ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        p.lse[static_cast<size_t>(zq) * p.Nq + row] = lse;
+        p.lse[static_cast<size_t>(it.zq) * p.Nq + row] = lse;
       }
-      // O row -> bf16 -> swizzled staging in this tile's (now idle) Q buffer.
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(it.zq) * p.Nq + row) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        if (have) {
+        if (n_kv > 0) {
           tmem_ld_32x32b_x32(t_o + c * 32, o);
           tmem_ld_wait();
         } else {
@@ -444,21 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        const uint32_t base = smem_u32(sm.q[x][c / 2]) + r * 128;
+        if (row < p.Nq) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ch = (c % 2) * 4 + i;
-          st_shared_v4(base + ((ch ^ (r & 7)) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1 + x);
-      if (r == 0) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tma_store_3d(&tm_o, sm.q[x][c], c * 64, m0 + x * kBM, zq);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-      }
+      tc_fence_before_sync();
     }
   }
 
@@ -470,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Drain what is still in flight before the CTA's memory goes away.
     if (warp == kWarpLoad && lane == 0) {
       for (int x = 0; x < 2; ++x)
-        if (issued_q[x]) mbar_wait(&sm.q_full[x], 0, p.wait_ns);
+        if (q_loads[x] > 0) mbar_wait(&sm.q_full[x], (q_loads[x] - 1) & 1, p.wait_ns);
       for (int s = 0; s < 2; ++s)
         if (issued_pairs[s] > 0) mbar_wait(&sm.full[s], (issued_pairs[s] - 1) & 1, p.wait_ns);
     }
@@ -495,9 +553,22 @@ size_t smem_bytes_for() {
   return s < 120 * 1024 ? 120 * 1024 : s;
 }
 
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int D>
 cudaError_t launch_d(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t stream) {
   KernelParams kp;
+  kp.out = static_cast<__nv_bfloat16*>(a.out);
   kp.lse = a.lse;
   kp.status = g.status;
   kp.wait_ns = g.wait_ns;
@@ -508,16 +579,20 @@ cudaError_t launch_d(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t st
   kp.group = a.Hq / a.Hkv;
   kp.n_ctiles = (a.Nq + 2 * kBM - 1) / (2 * kBM);
   kp.n_bh = a.B * a.Hq;
+  const long long n_items = static_cast<long long>(kp.n_ctiles) * kp.n_bh;
+  if (n_items > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+  kp.n_items = static_cast<int>(n_items);
   kp.causal = a.causal;
   kp.scale_log2 = a.scale * 1.4426950408889634f;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   const size_t smem = smem_bytes_for<D>();
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long n_cta = static_cast<long long>(kp.n_ctiles) * kp.n_bh;
-  if (n_cta > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-  dim3 grid(static_cast<unsigned>(n_cta));
-  prefill_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, kp);
+  // persistent: one CTA per SM (each holds all 512 TMEM columns)
+  const int grid = static_cast<int>(min(n_items, static_cast<long long>(sms)));
+  prefill_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, kp);
   return cudaGetLastError();
 }
 
