@@ -21,8 +21,10 @@
 //              and sum l, writes P (bf16) back into TMEM over S, rescales O
 //              in TMEM when m grows by more than kRescaleThreshold (log2
 //              units), and writes its O row and lse in the epilogue.
-//   warp 8     TMA producer: Q_A, Q_B per item, then K/V copies in pairs
-//              {V_(j-1), K_j} through a 4-slot ring.
+//   warp 8     TMA producer: Q tiles through a 3-buffer ring (so an item's
+//              Q_A can land while the previous item still runs), K/V copies
+//              in pairs {V_(j-1), K_j} through a 4-slot ring; an item's last
+//              V travels with the next item's K_0.
 //   warp 9     tcgen05 issuer (one thread), also owns the TMEM allocation.
 //              Issue order per key tile j:
 //                S_A = Q_A K_j^T,  O_B += P_B(j-1) V_(j-1),  S_B = Q_B K_j^T,
@@ -50,6 +52,7 @@ constexpr int kBN = 128;  // keys per tile
 constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kQBuf = 3;  // Q buffers: the next item's Q_A loads while this item runs
 constexpr int kRing = 4;  // K/V slots: K_j in slot 2j % 4, V_j in slot (2j+1) % 4
 // Copies travel in pairs: pair j = {V_(j-1), K_j} shares one completion
 // barrier and one release (pair slot j % 2): K_j and V_(j-1) are both done
@@ -62,9 +65,9 @@ constexpr uint32_t kSubTileBytes = 128 * 64 * 2;
 
 template <int D>
 struct alignas(1024) PrefillSmem {
-  uint8_t q[2][D / 64][kSubTileBytes];        // Q_A, Q_B; each reused as O staging
+  uint8_t q[kQBuf][D / 64][kSubTileBytes];     // Q tiles, a ring over the CTA's tiles
   uint8_t ring[kRing][D / 64][kSubTileBytes];  // K/V tiles
-  uint64_t q_full[2], q_free[2];  // Q tile landed / Q buffer no longer read
+  uint64_t q_full[kQBuf], q_free[kQBuf];  // Q tile landed / Q buffer no longer read
   uint64_t full[2], empty[2];  // per pair slot: pair j = {V_(j-1), K_j}
   uint64_t s_full[2], p_full[2], o_done[2], mma_fin;
   uint32_t tmem_base;
@@ -212,9 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    for (int b = 0; b < kQBuf; ++b) {
+      mbar_init(&sm.q_full[b], 1);
+      mbar_init(&sm.q_free[b], 1);
+    }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&sm.q_full[x], 1);
-      mbar_init(&sm.q_free[x], 1);
       mbar_init(&sm.s_full[x], 1);
       mbar_init(&sm.p_full[x], 128);
       mbar_init(&sm.o_done[x], 1);
@@ -237,82 +242,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
-  int issued_pairs[2] = {0, 0};  // producer: copy pairs issued per pair slot
-  int q_loads[2] = {0, 0};       // producer: Q tiles issued per buffer
+  int issued_pairs[2] = {0, 0};    // producer: copy pairs issued per pair slot
+  int q_loads[kQBuf] = {0, 0, 0};  // producer: Q tiles issued per buffer
   bool mma_issued = false;
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();  // K/V tiles are re-read by other CTAs
-      int g = 0;  // running pair index: pair g uses slot g & 1
+      int g = 0;   // running pair index: pair g uses pair slot g & 1
+      int qt = 0;  // running Q tile index: tile t uses buffer t % kQBuf
+      int v_zk = -1, v_tile = 0;  // the V tile owed by the next pair (v_zk < 0: none)
       bool ok = true;
+      // Pair g = {the owed V tile, K tile k_tile of plane k_zk (if k_zk >= 0)};
+      // the V tile with the same index as that K tile is owed next, so the
+      // last V of an item travels with the next item's K_0.
+      auto issue_pair = [&](int k_zk, int k_tile) -> bool {
+        const int ps = g & 1;
+        if (g >= 2 && !wait_or_abort(&sm.empty[ps], ((g >> 1) - 1) & 1, p, &sm.abort_flag)) return false;
+        const bool has_v = v_zk >= 0, has_k = k_zk >= 0;
+        mbar_arrive_expect_tx(&sm.full[ps], (has_v + has_k) * D * kBN * 2);
+        if (has_v) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_hint(sm.ring[(2 * g + 3) % kRing][c], &tm_v, &sm.full[ps], c * 64, v_tile * kBN,
+                             v_zk, keep);
+        }
+        if (has_k) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_hint(sm.ring[(2 * g) % kRing][c], &tm_k, &sm.full[ps], c * 64, k_tile * kBN, k_zk,
+                             keep);
+        }
+        issued_pairs[ps] = (g >> 1) + 1;
+        ++g;
+        v_zk = k_zk;
+        v_tile = k_tile;
+        return true;
+      };
       for (int round = 0; ok; ++round) {
         const int idx = item_index(round);
         if (idx >= p.n_items) break;
         const Item it = item_at(idx, p);
         if (it.n_iter == 0) continue;
-        for (int x = 0; x < 2 && ok; ++x) {
+        // The previous item's last V is needed before this item's Q.
+        if (!(ok = issue_pair(it.zk, 0))) break;
+        for (int x = 0; x < 2; ++x) {
           if (it.ti[x].n_kv == 0) continue;
+          const int b = qt % kQBuf;
           // the previous Q of this buffer must have been read by its last S
-          if (q_loads[x] > 0 && !wait_or_abort(&sm.q_free[x], (q_loads[x] - 1) & 1, p, &sm.abort_flag)) {
+          if (q_loads[b] > 0 && !wait_or_abort(&sm.q_free[b], (q_loads[b] - 1) & 1, p, &sm.abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.q_full[x], D * kBM * 2);
+          mbar_arrive_expect_tx(&sm.q_full[b], D * kBM * 2);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sm.q[x][c], &tm_q, &sm.q_full[x], c * 64, it.m0 + x * kBM, it.zq);
-          ++q_loads[x];
+            tma_load_3d(sm.q[b][c], &tm_q, &sm.q_full[b], c * 64, it.m0 + x * kBM, it.zq);
+          ++q_loads[b];
+          ++qt;
         }
-        for (int pp = 0; ok && pp <= it.n_iter; ++pp, ++g) {  // pair pp = {V_(pp-1), K_pp}
-          const int ps = g & 1;
-          if (g >= 2 && !wait_or_abort(&sm.empty[ps], ((g >> 1) - 1) & 1, p, &sm.abort_flag)) {
-            ok = false;
-            break;
-          }
-          const bool has_v = pp >= 1, has_k = pp < it.n_iter;
-          mbar_arrive_expect_tx(&sm.full[ps], (has_v + has_k) * D * kBN * 2);
-          if (has_v) {
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d_hint(sm.ring[(2 * g + 3) % kRing][c], &tm_v, &sm.full[ps], c * 64,
-                               (pp - 1) * kBN, it.zk, keep);
-          }
-          if (has_k) {
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-              tma_load_3d_hint(sm.ring[(2 * g) % kRing][c], &tm_k, &sm.full[ps], c * 64, pp * kBN,
-                               it.zk, keep);
-          }
-          issued_pairs[ps] = (g >> 1) + 1;
-        }
+        for (int j = 1; ok && j < it.n_iter; ++j) ok = issue_pair(it.zk, j);
       }
+      if (ok && v_zk >= 0) issue_pair(-1, 0);  // the last item's last V
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
-      // Descriptors are built once; a k-step, sub-tile or ring slot moves
-      // only the start-address field (units of 16 bytes, no carry: shared
-      // addresses stay below 2^18).
+      // Descriptors are built once; a k-step, sub-tile, Q buffer or ring
+      // slot moves only the start-address field (units of 16 bytes, no
+      // carry: shared addresses stay below 2^18).
       constexpr uint32_t kSlotUnits = (D / 64) * kSubTileBytes / 16;
-      const uint64_t dq[2] = {smem_desc(smem_u32(&sm.q[0][0][0]), 16, 1024, kSwizzle128B),
-                              smem_desc(smem_u32(&sm.q[1][0][0]), 16, 1024, kSwizzle128B)};
+      const uint64_t dq = smem_desc(smem_u32(&sm.q[0][0][0]), 16, 1024, kSwizzle128B);
       const uint64_t dk = smem_desc(smem_u32(&sm.ring[0][0][0]), 16, 1024, kSwizzle128B);
       const uint64_t dv = smem_desc(smem_u32(&sm.ring[0][0][0]), kSubTileBytes, 1024, kSwizzle128B);
-      int g = 0;                  // running pair index (as the producer's)
-      int q_waits[2] = {0, 0};    // completions of q_full[x] consumed
-      int p_waits[2] = {0, 0};    // completions of p_full[x] consumed
+      int g = 0;                          // running pair index (as the producer's)
+      int qt = 0;                         // running Q tile index (as the producer's)
+      int q_waits[kQBuf] = {0, 0, 0};     // completions of q_full[b] consumed
+      int p_waits[2] = {0, 0};            // completions of p_full[x] consumed
 
-      // S_X = Q_X K^T with K in the ring slot of running pair gk
-      auto qk = [&](int x, int gk) {
+      // S_X = Q_X K^T with Q_X in buffer qb and K in the ring slot of pair gk
+      auto qk = [&](int x, int qb, int gk) {
+        const uint64_t qd = dq + static_cast<uint64_t>(qb * kSlotUnits);
         const uint64_t kb = dk + static_cast<uint64_t>(((2 * gk) % kRing) * kSlotUnits);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
-          umma_bf16_ss(tmem + tmem_s_col(x), dq[x] + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + tmem_s_col(x), qd + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&sm.s_full[x]);
       };
@@ -330,9 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         return true;
       };
-      auto wait_q = [&](int x) -> bool {
-        if (!wait_or_abort(&sm.q_full[x], q_waits[x] & 1, p, &sm.abort_flag)) return false;
-        ++q_waits[x];
+      auto wait_q = [&](int qb) -> bool {
+        if (!wait_or_abort(&sm.q_full[qb], q_waits[qb] & 1, p, &sm.abort_flag)) return false;
+        ++q_waits[qb];
         tc_fence_after_sync();
         return true;
       };
@@ -344,15 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = item_at(idx, p);
         if (it.n_iter == 0) continue;
         const int nA = it.ti[0].n_kv, nB = it.ti[1].n_kv, n_iter = it.n_iter;
-        const int base = g;  // running index of this item's pair 0 = {K_0}
+        int qa = 0, qb = 0;  // Q buffers of tiles A and B
+        if (nA > 0) qa = qt++ % kQBuf;
+        if (nB > 0) qb = qt++ % kQBuf;
+        // Pair base = {previous item's last V, K_0}: already complete if a
+        // previous item waited for it.
+        const int base = g;
         if (!wait_or_abort(&sm.full[base & 1], (base >> 1) & 1, p, &sm.abort_flag)) break;
         tc_fence_after_sync();
         for (int j = 0; j <= n_iter; ++j) {
           // ---- S_A(j) = Q_A K_j^T   (K_j came with pair base + j)
           if (j < nA) {
-            if (j == 0 && !(ok = wait_q(0))) break;
-            qk(0, base + j);
-            if (j == nA - 1) umma_commit(&sm.q_free[0]);  // Q_A no longer read
+            if (j == 0 && !(ok = wait_q(qa))) break;
+            qk(0, qa, base + j);
+            if (j == nA - 1) umma_commit(&sm.q_free[qa]);  // Q_A no longer read
             mma_issued = true;
           }
           // ---- O_B += P_B(j-1) V_(j-1)
@@ -362,15 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j - 1 == nB - 1) umma_commit(&sm.o_done[1]);
             mma_issued = true;
           }
-          if (j == n_iter) {
-            umma_commit(&sm.empty[(base + j) & 1]);  // last pair {V_(n-1)} no longer read
-            break;
-          }
+          // Pair base + n_iter also carries the next item's K_0; that item
+          // releases it after its S_B(0).
+          if (j == n_iter) break;
           // ---- S_B(j) = Q_B K_j^T
           if (j < nB) {
-            if (j == 0 && !(ok = wait_q(1))) break;
-            qk(1, base + j);
-            if (j == nB - 1) umma_commit(&sm.q_free[1]);
+            if (j == 0 && !(ok = wait_q(qb))) break;
+            qk(1, qb, base + j);
+            if (j == nB - 1) umma_commit(&sm.q_free[qb]);
             mma_issued = true;
           }
           umma_commit(&sm.empty[(base + j) & 1]);  // pair {V_(j-1), K_j} no longer read
@@ -385,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_issued = true;
           }
         }
-        g = base + n_iter + 1;
+        g = base + n_iter;
       }
     }
   } else {
@@ -527,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (aborted) {
     // Drain what is still in flight before the CTA's memory goes away.
     if (warp == kWarpLoad && lane == 0) {
-      for (int x = 0; x < 2; ++x)
-        if (q_loads[x] > 0) mbar_wait(&sm.q_full[x], (q_loads[x] - 1) & 1, p.wait_ns);
+      for (int b = 0; b < kQBuf; ++b)
+        if (q_loads[b] > 0) mbar_wait(&sm.q_full[b], (q_loads[b] - 1) & 1, p.wait_ns);
       for (int s = 0; s < 2; ++s)
         if (issued_pairs[s] > 0) mbar_wait(&sm.full[s], (issued_pairs[s] - 1) & 1, p.wait_ns);
     }
