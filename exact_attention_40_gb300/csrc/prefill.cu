@@ -83,9 +83,11 @@ struct KernelParams {
   float scale_log2;  // scale * log2(e)
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              const KernelParams& p, uint32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of a bounded wait, kept out of line so that the fast path (one
+// try_wait) stays short in the issue loops.  Gives up after wait_ns, or at
+// once when another thread of the CTA has given up.
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, unsigned long long wait_ns,
+                                       unsigned int* status, uint32_t* abort_flag) {
   volatile uint32_t* ab = abort_flag;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
@@ -93,12 +95,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*ab) return false;
-    if (globaltimer_ns() - t0 > p.wait_ns) {
-      atomicOr(p.status, 1u);  // EXATTN_DEVICE_TIMEOUT_BIT
+    if (globaltimer_ns() - t0 > wait_ns) {
+      atomicOr(status, 1u);  // EXATTN_DEVICE_TIMEOUT_BIT
       *ab = 1u;
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              const KernelParams& p, uint32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, p.wait_ns, p.status, abort_flag);
 }
 
 // O (+)= P V with P (bf16, 128 x kBN) read from TMEM.
@@ -321,12 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;                          // running pair index (as the producer's)
       int qt = 0;                         // running Q tile index (as the producer's)
       int q_waits[kQBuf] = {0, 0, 0};     // completions of q_full[b] consumed
-      int p_waits[2] = {0, 0};            // completions of p_full[x] consumed
 
-      // S_X = Q_X K^T with Q_X in buffer qb and K in the ring slot of pair gk
-      auto qk = [&](int x, int qb, int gk) {
-        const uint64_t qd = dq + static_cast<uint64_t>(qb * kSlotUnits);
-        const uint64_t kb = dk + static_cast<uint64_t>(((2 * gk) % kRing) * kSlotUnits);
+      // Pair g carries K_j and V_(j-1): K in ring slot (2g) % 4, V in slot
+      // (2g + 3) % 4, i.e. slots 0 and 3 for even g, 2 and 1 for odd g.
+      const uint64_t dk_even = dk, dk_odd = dk + 2 * kSlotUnits;
+      const uint64_t dv_even = dv + 3 * kSlotUnits, dv_odd = dv + kSlotUnits;
+      int p_waits0 = 0, p_waits1 = 0;  // completions of p_full[0], p_full[1] consumed
+
+      // S_X = Q_X K^T (Q_X at descriptor qd, K at kb), then signal s_full[X]
+      auto qk = [&](int x, uint64_t qd, uint64_t kb) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
@@ -334,19 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&sm.s_full[x]);
       };
-      // O_X (+)= P_X V with V in the ring slot of running pair gv
-      auto pv = [&](int x, int gv, bool first) {
-        const uint64_t vb = dv + static_cast<uint64_t>(((2 * gv + 3) % kRing) * kSlotUnits);
+      // O_X (+)= P_X V with V at vb; acc0 = 0 starts O_X afresh
+      auto pv = [&](int x, uint64_t vb, uint32_t acc0) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           umma_bf16_ts(tmem + tmem_o_col(x), tmem + tmem_s_col(x) + kk * 8, vb + kk * 128, id_pv,
-                       (!first || kk > 0) ? 1u : 0u);
-      };
-      auto wait_p = [&](int x) -> bool {
-        if (!wait_or_abort(&sm.p_full[x], p_waits[x] & 1, p, &sm.abort_flag)) return false;
-        ++p_waits[x];
-        tc_fence_after_sync();
-        return true;
+                       kk > 0 ? 1u : acc0);
       };
       auto wait_q = [&](int qb) -> bool {
         if (!wait_or_abort(&sm.q_full[qb], q_waits[qb] & 1, p, &sm.abort_flag)) return false;
@@ -365,25 +369,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         int qa = 0, qb = 0;  // Q buffers of tiles A and B
         if (nA > 0) qa = qt++ % kQBuf;
         if (nB > 0) qb = qt++ % kQBuf;
+        const uint64_t qd_a = dq + static_cast<uint64_t>(qa * kSlotUnits);
+        const uint64_t qd_b = dq + static_cast<uint64_t>(qb * kSlotUnits);
+        mma_issued = true;
         // Pair base = {previous item's last V, K_0}: already complete if a
         // previous item waited for it.
         const int base = g;
         if (!wait_or_abort(&sm.full[base & 1], (base >> 1) & 1, p, &sm.abort_flag)) break;
         tc_fence_after_sync();
         for (int j = 0; j <= n_iter; ++j) {
-          // ---- S_A(j) = Q_A K_j^T   (K_j came with pair base + j)
+          const int gk = base + j;  // pair of K_j and V_(j-1)
+          const bool odd = (gk & 1) != 0;
+          const uint64_t kb = odd ? dk_odd : dk_even;
+          const uint64_t vb_prev = odd ? dv_odd : dv_even;
+          const uint64_t vb_next = odd ? dv_even : dv_odd;  // V_j, in pair gk + 1
+          // ---- S_A(j) = Q_A K_j^T
           if (j < nA) {
             if (j == 0 && !(ok = wait_q(qa))) break;
-            qk(0, qa, base + j);
+            qk(0, qd_a, kb);
             if (j == nA - 1) umma_commit(&sm.q_free[qa]);  // Q_A no longer read
-            mma_issued = true;
           }
           // ---- O_B += P_B(j-1) V_(j-1)
           if (j >= 1 && j - 1 < nB) {
-            if (!(ok = wait_p(1))) break;
-            pv(1, base + j, j == 1);
+            if (!(ok = wait_or_abort(&sm.p_full[1], p_waits1 & 1, p, &sm.abort_flag))) break;
+            ++p_waits1;
+            tc_fence_after_sync();
+            pv(1, vb_prev, j == 1 ? 0u : 1u);
             if (j - 1 == nB - 1) umma_commit(&sm.o_done[1]);
-            mma_issued = true;
           }
           // Pair base + n_iter also carries the next item's K_0; that item
           // releases it after its S_B(0).
@@ -391,20 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           // ---- S_B(j) = Q_B K_j^T
           if (j < nB) {
             if (j == 0 && !(ok = wait_q(qb))) break;
-            qk(1, qb, base + j);
+            qk(1, qd_b, kb);
             if (j == nB - 1) umma_commit(&sm.q_free[qb]);
-            mma_issued = true;
           }
-          umma_commit(&sm.empty[(base + j) & 1]);  // pair {V_(j-1), K_j} no longer read
-          // ---- pair base+j+1 = {V_j, K_(j+1)}, then O_A += P_A(j) V_j
-          const int gn = base + j + 1;
+          umma_commit(&sm.empty[gk & 1]);  // pair {V_(j-1), K_j} no longer read
+          // ---- pair gk+1 = {V_j, K_(j+1)}, then O_A += P_A(j) V_j (one fence
+          // after both waits)
+          const int gn = gk + 1;
           if (!(ok = wait_or_abort(&sm.full[gn & 1], (gn >> 1) & 1, p, &sm.abort_flag))) break;
-          tc_fence_after_sync();
           if (j < nA) {
-            if (!(ok = wait_p(0))) break;
-            pv(0, gn, j == 0);
+            if (!(ok = wait_or_abort(&sm.p_full[0], p_waits0 & 1, p, &sm.abort_flag))) break;
+            ++p_waits0;
+            tc_fence_after_sync();
+            pv(0, vb_next, j == 0 ? 0u : 1u);
             if (j == nA - 1) umma_commit(&sm.o_done[0]);
-            mma_issued = true;
+          } else {
+            tc_fence_after_sync();
           }
         }
         g = base + n_iter;
