@@ -280,3 +280,35 @@ def sample_rows(seed: int, B: int, Hq: int, Nq: int, per_head: int) -> np.ndarra
             for i in sorted(chosen):
                 rows.append((b, h, i))
     return np.asarray(rows, np.int64).reshape(-1, 3)
+
+
+# ------------------------------------------------------------ add_rms_norm
+@dataclass(frozen=True)
+class NormConfig:
+    name: str
+    rows: int    # tokens
+    hidden: int
+    seed: int
+    eps: float = 1e-6
+
+
+# The shape the fusion page measures add_rms_norm on ((64, 8192) bf16), and a
+# large batch of the same hidden size that streams far more than L2 holds.
+NORM = {
+    "rmsnorm_64x8192": NormConfig("rmsnorm_64x8192", 64, 8192, 6),
+    "rmsnorm_16384x8192": NormConfig("rmsnorm_16384x8192", 16384, 8192, 7),
+}
+
+
+def norm_inputs_shape(seed: int, rows: int, hidden: int):
+    """x, residual ~ N(0,1) bf16 [rows, hidden]; weight = 1 + 0.1 N(0,1) bf16
+    [hidden] (a learned RMSNorm gain sits near one; the page gives none)."""
+    x = normal_bf16(seed, 0, (rows, hidden))
+    r = normal_bf16(seed, 1, (rows, hidden))
+    z = bf16_bits_to_f32(normal_bf16(seed, 2, (hidden,))).astype(np.float64)
+    w = f32_to_bf16_bits((1.0 + 0.1 * z).astype(np.float32))
+    return x, r, w
+
+
+def norm_inputs(cfg: NormConfig):
+    return norm_inputs_shape(cfg.seed, cfg.rows, cfg.hidden)

@@ -57,6 +57,8 @@ def _load():
     lib.oracle_softmax_f64.restype = None
     lib.oracle_online_softmax_f64.argtypes = [P, L, P]
     lib.oracle_online_softmax_f64.restype = None
+    lib.oracle_add_rms_norm_f64.argtypes = [P, P, P, L, L, D, P, P]
+    lib.oracle_add_rms_norm_f64.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     lib.oracle_set_num_threads.argtypes = [I]
@@ -156,3 +158,21 @@ def online_softmax(x):
     y = np.empty_like(x)
     _load().oracle_online_softmax_f64(_ptr(x), x.size, _ptr(y))
     return y
+
+
+def add_rms_norm(x, residual, weight, eps: float):
+    """Residual add + RMS normalisation.  x, residual [T, D], weight [D]
+    (uint16 bf16 bits).
+
+    Returns (out fp64 [T, D], new residual h = x + residual fp64 [T, D])."""
+    x, residual, weight = _u16(x), _u16(residual), _u16(weight)
+    if x.ndim != 2 or residual.shape != x.shape or weight.shape != (x.shape[1],):
+        raise ValueError("shape mismatch")
+    T, D = x.shape
+    out = np.zeros((T, D), np.float64)
+    h = np.zeros((T, D), np.float64)
+    rc = _load().oracle_add_rms_norm_f64(_ptr(x), _ptr(residual), _ptr(weight), T, D, float(eps),
+                                         _ptr(out), _ptr(h))
+    if rc != 0:
+        raise ValueError("oracle_add_rms_norm_f64 rejected its arguments")
+    return out, h

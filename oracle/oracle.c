@@ -34,6 +34,9 @@
  *     current token, which is already in the cache.
  *
  * Inputs are bf16 bit patterns (uint16), widened exactly to fp64.
+ *
+ * Also here: the residual add + RMS normalisation that sits next to
+ * attention in every layer (oracle_add_rms_norm_f64, at the end).
  */
 #include <math.h>
 #include <stdint.h>
@@ -277,4 +280,37 @@ void oracle_online_softmax_f64(const double* x, long n, double* y) {
     m = m_new;
   }
   for (j = 0; j < n; ++j) y[j] = exp(x[j] - m) / dsum;
+}
+
+/* Residual add + RMS normalisation of n_rows rows of `hidden` values each
+ * ("Inference Engineering VII.07: Kernel and Operator Fusion" page,
+ * section 4, the unfused form and the steps of the fused kernel; section 5,
+ * why the kernel returns the new residual as well):
+ *
+ *   h_i   = x_i + r_i                        the new residual
+ *   ms    = (1 / hidden) * sum_i h_i^2       mean of squares over the row
+ *   out_i = h_i / sqrt(ms + eps) * w_i
+ *
+ * x, r: [n_rows, hidden], w: [hidden], bf16 bit patterns widened exactly to
+ * fp64; out, h_out: [n_rows, hidden] fp64.  Nothing is rounded.  Returns
+ * nonzero for a bad argument. */
+int oracle_add_rms_norm_f64(const uint16_t* x, const uint16_t* r, const uint16_t* w, long n_rows,
+                            long hidden, double eps, double* out, double* h_out) {
+  if (n_rows < 0 || hidden < 1 || !(eps >= 0.0)) return 1;
+#pragma omp parallel for schedule(static)
+  for (long row = 0; row < n_rows; ++row) {
+    const uint16_t* xr = x + row * hidden;
+    const uint16_t* rr = r + row * hidden;
+    double* hr = h_out + row * hidden;
+    double ss = 0.0;
+    for (long i = 0; i < hidden; ++i) {
+      hr[i] = bf16_to_f64(xr[i]) + bf16_to_f64(rr[i]);
+      ss += hr[i] * hr[i];
+    }
+    const double ms = ss / (double)hidden;
+    const double denom = sqrt(ms + eps);
+    double* o = out + row * hidden;
+    for (long i = 0; i < hidden; ++i) o[i] = hr[i] / denom * bf16_to_f64(w[i]);
+  }
+  return 0;
 }

@@ -21,6 +21,10 @@ def digests():
     table, nb = synth.paged_layout(lens, 16, 5)
     out["decode_paged.block_table"] = hashlib.sha256(table.tobytes()).hexdigest()
     out["decode_paged.num_blocks"] = int(nb)
+    x, r, w = synth.norm_inputs(synth.NORM["rmsnorm_64x8192"])
+    for name, a in (("rmsnorm_64x8192.x", x), ("rmsnorm_64x8192.residual", r),
+                    ("rmsnorm_64x8192.weight", w)):
+        out[name] = hashlib.sha256(a.tobytes()).hexdigest()
     return out
 
 
