@@ -326,11 +326,62 @@ def run_gpu(args):
                "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
                "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4}
 
+    # ---- add_rms_norm: the residual add + RMS normalisation next to
+    # attention in each layer, timed apart from the attention step (not in
+    # value or ms_per_step); L2 flushed before every call, and the page's
+    # shape also back to back (warm: its 4 MB stay in L2).
+    norm = None
+    if args.norm_calls > 0:
+        norm = {}
+        for key, calls in (("rmsnorm_64x8192", args.norm_calls),
+                           ("rmsnorm_16384x8192", max(3, args.norm_calls // 20))):
+            nc = synth.NORM[key]
+            xn, rn, wn = synth.norm_inputs(nc)
+            xd, rd, wd = to_dev(xn), to_dev(rn), to_dev(wn)
+            od, hd = torch.empty_like(xd), torch.empty_like(xd)
+            for _ in range(3):
+                exattn.attn_add_rms_norm(xd, rd, wd, nc.eps, out=od, residual_out=hd)
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(calls)]
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                exattn.attn_add_rms_norm(xd, rd, wd, nc.eps, out=od, residual_out=hd)
+                e1.record(stream)
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0.record(stream)
+            for _ in range(calls):
+                exattn.attn_add_rms_norm(xd, rd, wd, nc.eps, out=od, residual_out=hd)
+            w1.record(stream)
+            torch.cuda.synchronize()
+            if exattn.attn_get_device_status() != 0:
+                raise RuntimeError("device status word set by add_rms_norm")
+            ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / calls
+            ms_warm = w0.elapsed_time(w1) / calls
+            nbytes = 4 * nc.rows * nc.hidden * 2 + nc.hidden * 2
+            norm[key] = {"shape": [nc.rows, nc.hidden], "us": ms * 1e3, "us_warm": ms_warm * 1e3,
+                         "gbs": nbytes / (ms * 1e-3) / 1e9,
+                         "frac_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+                         "bytes": nbytes, "calls": calls}
+            del xd, rd, wd, od, hd
+        norm["context"] = ("the fusion page measures 142 us unfused, 41 us fused at (64, 8192) "
+                           "bf16 on hardware it does not state")
+
     if rank != 0:
         return 0
     cpu = None if args.no_cpu_baseline else cpu_baseline_leg()
     traffic = load_traffic("prefill.cu", "prefill_llama3_8b_causal")
     dtraffic = load_traffic("decode.cu", "decode_split_decode_paged")
+    if norm is not None:
+        big = norm["rmsnorm_16384x8192"]
+        line_norm = {"kernel": "add_rms_norm_kernel<4>", "bound": "hbm", "achieved": big["gbs"],
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": big["gbs"] / peaks["hbm"],
+                     "peak_kind": "HBM copy (%s)" % peaks["src"],
+                     "workload": "rmsnorm_16384x8192",
+                     "traffic": load_traffic("norm.cu", "add_rms_norm_16384x8192")}
+    else:
+        line_norm = None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -348,6 +399,7 @@ def run_gpu(args):
         "roofline": {"kernel": "prefill_kernel<128>", "bound": "tensor", "achieved": achieved,
                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
                      "peak_kind": "bf16 burst (%s)" % peaks["src"], "traffic": traffic},
+        "roofline_norm": line_norm,
         "roofline_decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                             "bound": "hbm", "achieved": decode_bytes / (dec_avg_ms * 1e-3) / 1e9,
                             "peak": peaks["hbm"], "unit": "GB/s",
@@ -355,6 +407,7 @@ def run_gpu(args):
                             "peak_kind": "HBM copy (%s)" % peaks["src"], "traffic": dtraffic},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "add_rms_norm": norm,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
@@ -370,6 +423,8 @@ def main():
     ap.add_argument("--impl", default="exattn", choices=["exattn", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--norm-calls", type=int, default=200,
+                    help="add_rms_norm calls per shape (0 skips that measurement)")
     ap.add_argument("--ref-rows-total", type=int, default=60000,
                     help="reference arm: query rows spread over all steps")
     args = ap.parse_args()

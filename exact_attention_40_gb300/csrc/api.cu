@@ -316,6 +316,32 @@ int attn_decode_paged_static(const void* q, const void* k_cache, const void* v_c
                            EXATTN_STATIC_SCRATCH_BYTES, stream);
 }
 
+int attn_add_rms_norm(const void* x, const void* residual, const void* weight, void* out,
+                      void* residual_out, int n_rows, int hidden, float eps, void* stream) {
+  if (n_rows < 0 || hidden < 1 || !(eps >= 0.f) || !std::isfinite(eps)) return EXATTN_ERR_INVALID_ARG;
+  if (hidden % 8 != 0 || hidden > exattn::kNormMaxHidden) return EXATTN_ERR_UNSUPPORTED;
+  if (n_rows == 0) return EXATTN_OK;
+  if (x == nullptr || residual == nullptr || weight == nullptr || out == nullptr || residual_out == nullptr)
+    return EXATTN_ERR_INVALID_ARG;
+  if (out == residual_out || out == weight || residual_out == weight) return EXATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(weight) || !aligned16(out) ||
+      !aligned16(residual_out))
+    return EXATTN_ERR_ALIGNMENT;
+  exattn::NormArgs a;
+  a.x = x;
+  a.residual = residual;
+  a.weight = weight;
+  a.out = out;
+  a.residual_out = residual_out;
+  a.n_rows = n_rows;
+  a.hidden = hidden;
+  a.inv_hidden = 1.0f / static_cast<float>(hidden);
+  a.eps = eps;
+  if (exattn::launch_add_rms_norm(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXATTN_ERR_CUDA;
+  return EXATTN_OK;
+}
+
 int attn_get_device_status(void* stream, unsigned int* status_out) {
   if (status_out == nullptr) return EXATTN_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;

@@ -49,4 +49,20 @@ struct DecodeArgs {
 
 cudaError_t launch_decode(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t stream);
 
+struct NormArgs {
+  const void* x;          // [n_rows, hidden] bf16
+  const void* residual;   // [n_rows, hidden] bf16
+  const void* weight;     // [hidden] bf16
+  void* out;              // [n_rows, hidden] bf16
+  void* residual_out;     // [n_rows, hidden] bf16: x + residual
+  long long n_rows;
+  int hidden;             // multiple of 8, at most kNormMaxHidden
+  float inv_hidden;       // 1 / hidden
+  float eps;
+};
+
+constexpr int kNormMaxHidden = 16384;
+
+cudaError_t launch_add_rms_norm(const NormArgs& a, cudaStream_t stream);
+
 }  // namespace exattn

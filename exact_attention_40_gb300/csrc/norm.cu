@@ -1,0 +1,150 @@
+// Residual add + RMS normalisation for sm_103a.
+//
+// For each row of `hidden` bf16 values ("Inference Engineering VII.07:
+// Kernel and Operator Fusion" page, section 4 and the fused-kernel
+// structure of sections 6-9):
+//   h   = x + residual                       returned: the next residual
+//   out = h * rsqrt(mean(h^2) + eps) * weight
+// with two reads and two writes of the row and nothing in between: one CTA
+// holds a row in registers (16-byte vector loads), adds in fp32, reduces
+// the sum of squares by warp shuffles and then across the CTA's warps in
+// shared memory (every thread sums the warp totals in the same order, so
+// all threads hold the same factor), and stores both outputs as bf16
+// (round to nearest even).  HBM-bound: 4 x rows x hidden x 2 bytes plus the
+// weight per launch.
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace exattn {
+namespace {
+
+constexpr int kNormThreads = 256;
+constexpr int kNormWarps = kNormThreads / 32;
+
+// x and residual are read once: keep them out of L1.  The weight is shared
+// by every row and stays on the default path.
+__device__ __forceinline__ uint4 ld_once(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_once(uint4* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// VPT: 8-value vectors per thread per tensor; a row has nvec = hidden / 8
+// vectors, vector v of the row belongs to thread v % 256.
+template <int VPT>
+__global__ void __launch_bounds__(kNormThreads) add_rms_norm_kernel(const NormArgs a) {
+  __shared__ float warp_ss[kNormWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint4* x = static_cast<const uint4*>(a.x);
+  const uint4* r = static_cast<const uint4*>(a.residual);
+  const uint4* w = static_cast<const uint4*>(a.weight);
+  uint4* out = static_cast<uint4*>(a.out);
+  uint4* h_out = static_cast<uint4*>(a.residual_out);
+  const int nvec = a.hidden / 8;
+  for (long long row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
+    const size_t base = static_cast<size_t>(row) * nvec;
+    uint4 xv[VPT], rv[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * kNormThreads;
+      if (v < nvec) {
+        xv[i] = ld_once(x + base + v);
+        rv[i] = ld_once(r + base + v);
+      }
+    }
+    float h[VPT][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * kNormThreads;
+      if (v < nvec) {
+        float fx[8], fr[8];
+        unpack8(xv[i], fx);
+        unpack8(rv[i], fr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          h[i][e] = fx[e] + fr[e];
+          ss = fmaf(h[i][e], h[i][e], ss);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) warp_ss[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < kNormWarps; ++k) tot += warp_ss[k];
+    const float inv = rsqrtf(tot * a.inv_hidden + a.eps);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * kNormThreads;
+      if (v < nvec) {
+        float fw[8], o[8];
+        unpack8(__ldg(w + v), fw);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = h[i][e] * inv * fw[e];
+        st_once(out + base + v, pack8(o));
+        st_once(h_out + base + v, pack8(h[i]));
+      }
+    }
+    __syncthreads();  // warp_ss is refilled for the next row
+  }
+}
+
+int norm_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+cudaError_t launch_add_rms_norm(const NormArgs& a, cudaStream_t stream) {
+  const int nvec = a.hidden / 8;
+  const int sms = norm_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  // Eight 256-thread CTAs fit an SM; more rows than that are walked by a
+  // grid-stride loop.
+  const long long cap = static_cast<long long>(sms) * 8;
+  const int grid = static_cast<int>(a.n_rows < cap ? a.n_rows : cap);
+  const int vpt = (nvec + kNormThreads - 1) / kNormThreads;
+  if (vpt <= 1) add_rms_norm_kernel<1><<<grid, kNormThreads, 0, stream>>>(a);
+  else if (vpt <= 2) add_rms_norm_kernel<2><<<grid, kNormThreads, 0, stream>>>(a);
+  else if (vpt <= 4) add_rms_norm_kernel<4><<<grid, kNormThreads, 0, stream>>>(a);
+  else if (vpt <= 8) add_rms_norm_kernel<8><<<grid, kNormThreads, 0, stream>>>(a);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace exattn

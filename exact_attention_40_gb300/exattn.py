@@ -49,6 +49,8 @@ lib.attn_decode_split_tokens.argtypes = []
 lib.attn_decode_split_tokens.restype = _I
 lib.attn_debug_expire_wait.argtypes = [ctypes.c_ulonglong, _P]
 lib.attn_debug_expire_wait.restype = _I
+lib.attn_add_rms_norm.argtypes = [_P, _P, _P, _P, _P, _I, _I, _F, _P]
+lib.attn_add_rms_norm.restype = _I
 lib.attn_shutdown.argtypes = []
 lib.attn_shutdown.restype = None
 
@@ -165,6 +167,39 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, ctx_lens, scale: float |
     if rc != EXATTN_OK:
         raise ExattnError("attn_decode_paged", rc)
     return out, lse
+
+
+def attn_add_rms_norm(x, residual, weight, eps: float = 1e-6, out=None, residual_out=None,
+                      stream=None):
+    """Residual add + RMS normalisation.  x, residual [T, D] bf16; weight [D]
+    bf16; contiguous.  out / residual_out may be x or residual (in place).
+
+    Returns (out [T, D] bf16, residual_out = x + residual [T, D] bf16)."""
+    import torch
+    _check_tensor("x", x, torch.bfloat16, 2)
+    _check_tensor("residual", residual, torch.bfloat16, 2)
+    _check_tensor("weight", weight, torch.bfloat16, 1)
+    T, D = x.shape
+    if tuple(residual.shape) != (T, D) or tuple(weight.shape) != (D,):
+        raise ValueError("shape mismatch: x %s residual %s weight %s"
+                         % (tuple(x.shape), tuple(residual.shape), tuple(weight.shape)))
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _check_tensor("out", out, torch.bfloat16, 2)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    else:
+        _check_tensor("residual_out", residual_out, torch.bfloat16, 2)
+    if tuple(out.shape) != (T, D) or tuple(residual_out.shape) != (T, D):
+        raise ValueError("output shape mismatch")
+    with torch.cuda.device(x.device):
+        rc = lib.attn_add_rms_norm(x.data_ptr(), residual.data_ptr(), weight.data_ptr(),
+                                   out.data_ptr(), residual_out.data_ptr(), T, D, float(eps),
+                                   _stream_handle(stream))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_add_rms_norm", rc)
+    return out, residual_out
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -153,6 +153,29 @@ int attn_decode_paged_static(const void* q, const void* k_cache, const void* v_c
                              int num_blocks, int max_blocks_per_seq, float scale, void* stream);
 
 /*
+ * Residual add + RMS normalisation, the fusion that sits next to attention
+ * in every layer ("Inference Engineering VII.07: Kernel and Operator
+ * Fusion" page, section 4: the fused kernel loads x and the residual once,
+ * adds, reduces the sum of squares, scales, and stores both results;
+ * section 5: the sum is returned because the next layer's residual add
+ * needs it).  For each of n_rows rows of `hidden` values:
+ *   residual_out = x + residual
+ *   out          = residual_out * rsqrt(mean(residual_out^2) + eps) * weight
+ * with the sum, the mean of squares and the products in fp32 and each
+ * output rounded once to bf16 (nearest even).
+ *   x, residual, out, residual_out  [n_rows, hidden] bf16, row-major
+ *   weight                          [hidden] bf16
+ * hidden must be a multiple of 8 in [8, 16384]; eps finite and >= 0;
+ * n_rows >= 0 (0 launches nothing; pointers may then be NULL).  Every
+ * pointer 16-byte aligned.  out and residual_out may each be the same
+ * pointer as x or residual (in place), but not each other and not weight;
+ * no other overlap is allowed.  The caller owns every buffer.  One kernel
+ * launch on `stream`, asynchronous; deterministic.
+ */
+int attn_add_rms_norm(const void* x, const void* residual, const void* weight, void* out,
+                      void* residual_out, int n_rows, int hidden, float eps, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the status word of the
  * current device: 0, or an OR of EXATTN_DEVICE_*_BIT.  Returns EXATTN_OK
  * or EXATTN_ERR_CUDA.

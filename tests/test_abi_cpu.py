@@ -126,3 +126,26 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def norm(lib, x=FAKE, r=FAKE + 16, w=FAKE + 32, out=FAKE + 48, h=FAKE + 64, rows=4, hidden=64,
+         eps=1e-6):
+    return lib.lib.attn_add_rms_norm(x, r, w, out, h, rows, hidden, eps, None)
+
+
+def test_add_rms_norm_rejections(lib):
+    assert norm(lib, hidden=12) == 2
+    assert norm(lib, hidden=16392) == 2
+    assert norm(lib, hidden=0) == 1
+    assert norm(lib, rows=-1) == 1
+    assert norm(lib, eps=-1.0) == 1
+    assert norm(lib, eps=float("nan")) == 1
+    assert norm(lib, eps=float("inf")) == 1
+    assert norm(lib, x=None) == 1
+    assert norm(lib, h=None) == 1
+    assert norm(lib, out=FAKE + 48, h=FAKE + 48) == 1   # both outputs in one buffer
+    assert norm(lib, out=FAKE + 32) == 1                # output over the weight
+    assert norm(lib, r=FAKE + 8) == 3
+    assert norm(lib, out=FAKE + 50) == 3
+    # nothing to do: success without touching the (null) pointers
+    assert norm(lib, rows=0, x=None, r=None, w=None, out=None, h=None) == 0
