@@ -59,6 +59,8 @@ def _load():
     lib.oracle_online_softmax_f64.restype = None
     lib.oracle_add_rms_norm_f64.argtypes = [P, P, P, L, L, D, P, P]
     lib.oracle_add_rms_norm_f64.restype = I
+    lib.oracle_rope_cache_write_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D, P, P, P]
+    lib.oracle_rope_cache_write_f64.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     lib.oracle_set_num_threads.argtypes = [I]
@@ -176,3 +178,28 @@ def add_rms_norm(x, residual, weight, eps: float):
     if rc != 0:
         raise ValueError("oracle_add_rms_norm_f64 rejected its arguments")
     return out, h
+
+
+def rope_cache_write(q, k, seq_ids, positions, block_table, num_blocks: int, base: float):
+    """Rotary embedding of q [T, Hq, d] and k [T, Hkv, d] (uint16 bf16 bits)
+    at positions[t], and the cache slot each token's key and value go to.
+
+    Returns (q_out fp64 [T, Hq, d], k_out fp64 [T, Hkv, d], slot int64 [T]:
+    physical block * 16 + slot, -1 when outside the table or the cache)."""
+    q, k = _u16(q), _u16(k)
+    sid = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    T, Hq, d = q.shape
+    Tk, Hkv, dk = k.shape
+    if Tk != T or dk != d or sid.shape != (T,) or pos.shape != (T,) or bt.ndim != 2:
+        raise ValueError("shape mismatch")
+    q_out = np.zeros((T, Hq, d), np.float64)
+    k_out = np.zeros((T, Hkv, d), np.float64)
+    slot = np.zeros((T,), np.int64)
+    rc = _load().oracle_rope_cache_write_f64(_ptr(q), _ptr(k), _ptr(sid), _ptr(pos), _ptr(bt), T, Hq,
+                                             Hkv, d, bt.shape[0], int(num_blocks), bt.shape[1],
+                                             float(base), _ptr(q_out), _ptr(k_out), _ptr(slot))
+    if rc != 0:
+        raise ValueError("oracle_rope_cache_write_f64 rejected its arguments")
+    return q_out, k_out, slot

@@ -314,3 +314,60 @@ int oracle_add_rms_norm_f64(const uint16_t* x, const uint16_t* r, const uint16_t
   }
   return 0;
 }
+
+/* Rotary position embedding of the new tokens' queries and keys, then the
+ * store of the rotated key and the value into the block-paged cache
+ * ("Inference Engineering VII.07: Kernel and Operator Fusion" page,
+ * section 2, catalogue item "rope + cache write: RoPE then KV store";
+ * "Fused Kernel Compiler" page, table of fusion patterns, "RoPE embedding:
+ * sin, cos, rotate"; the cache layout of the "Optimizing LLM Inference ..."
+ * page, section Paged Attention and Dynamic KV Cache Management).
+ *
+ * Readings (the pages name the operation only): pairs (i, i + d/2) of each
+ * head vector are rotated by theta_i = pos * base^(-2 i / d),
+ *   y_i       = x_i cos theta_i - x_(i+d/2) sin theta_i
+ *   y_(i+d/2) = x_(i+d/2) cos theta_i + x_i sin theta_i,
+ * for i in [0, d/2); token t of sequence seq_ids[t] at position
+ * positions[t] goes to physical block block_table[seq][pos / 16], slot
+ * pos % 16.
+ *
+ * q [T, Hq, d], k, v [T, Hkv, d] bf16 bits; q_out [T, Hq, d], k_out
+ * [T, Hkv, d] fp64 (v is stored unchanged); slot_out [T]: block * 16 +
+ * slot, or -1 when the position or the block lies outside the table or the
+ * cache (nothing is stored then).  Returns nonzero for a bad argument. */
+static void rope_vec(const uint16_t* x, int d, long pos, double base, double* y) {
+  const int half = d / 2;
+  for (int i = 0; i < half; ++i) {
+    const double ang = (double)pos * pow(base, -2.0 * (double)i / (double)d);
+    const double c = cos(ang), s = sin(ang);
+    const double a = bf16_to_f64(x[i]), b = bf16_to_f64(x[i + half]);
+    y[i] = a * c - b * s;
+    y[i + half] = b * c + a * s;
+  }
+}
+
+int oracle_rope_cache_write_f64(const uint16_t* q, const uint16_t* k, const int32_t* seq_ids,
+                                const int32_t* positions, const int32_t* block_table, int T,
+                                int Hq, int Hkv, int d, int num_seqs, int num_blocks,
+                                int max_blocks_per_seq, double base, double* q_out, double* k_out,
+                                long* slot_out) {
+  if (T < 0 || Hq < 1 || Hkv < 1 || d < 2 || d % 2 != 0 || num_blocks < 0 || max_blocks_per_seq < 0 ||
+      !(base > 0.0))
+    return 1;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const long pos = positions[t];
+    const int seq = seq_ids[t];
+    for (int h = 0; h < Hq; ++h)
+      rope_vec(q + ((long)t * Hq + h) * d, d, pos, base, q_out + ((long)t * Hq + h) * d);
+    for (int h = 0; h < Hkv; ++h)
+      rope_vec(k + ((long)t * Hkv + h) * d, d, pos, base, k_out + ((long)t * Hkv + h) * d);
+    long slot = -1;
+    if (seq >= 0 && seq < num_seqs && pos >= 0 && pos / 16 < max_blocks_per_seq) {
+      const long blk = block_table[(long)seq * max_blocks_per_seq + pos / 16];
+      if (blk >= 0 && blk < num_blocks) slot = blk * 16 + pos % 16;
+    }
+    slot_out[t] = slot;
+  }
+  return 0;
+}
