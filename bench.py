@@ -368,6 +368,59 @@ def run_gpu(args):
         norm["context"] = ("the fusion page measures 142 us unfused, 41 us fused at (64, 8192) "
                            "bf16 on hardware it does not state")
 
+    # ---- RoPE + paged KV-cache write: the step before decode (rotates the
+    # new tokens' q and k, stores k and v into the paged cache), timed apart
+    # from the attention step like add_rms_norm.  The decode step writes into
+    # the decode workload's own caches (same block table).
+    rope = None
+    if args.rope_calls > 0:
+        rope = {}
+        for key, calls in (("rope_decode_step", args.rope_calls),
+                           ("rope_prefill_16k", max(3, args.rope_calls // 10))):
+            rc_ = synth.ROPE[key]
+            ri = synth.rope_inputs(rc_)
+            rq, rk, rv = to_dev(ri["q"]), to_dev(ri["k"]), to_dev(ri["v"])
+            rsid, rpos, rbt = to_dev(ri["seq_ids"]), to_dev(ri["positions"]), to_dev(ri["block_table"])
+            if key == "rope_decode_step":
+                rkc, rvc = dk, dv
+            else:
+                shape = (ri["num_blocks"], rc_.Hkv, 16, rc_.d)
+                rkc = torch.zeros(shape, device=dev, dtype=torch.bfloat16)
+                rvc = torch.zeros(shape, device=dev, dtype=torch.bfloat16)
+
+            def rope_call():
+                exattn.attn_rope_cache_write(rq, rk, rv, rsid, rpos, rbt, rkc, rvc, base=rc_.base)
+
+            for _ in range(3):
+                rope_call()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(calls)]
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                rope_call()
+                e1.record(stream)
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0.record(stream)
+            for _ in range(calls):
+                rope_call()
+            w1.record(stream)
+            torch.cuda.synchronize()
+            if exattn.attn_get_device_status() != 0:
+                raise RuntimeError("device status word set by attn_rope_cache_write")
+            ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / calls
+            ms_warm = w0.elapsed_time(w1) / calls
+            T = int(ri["positions"].shape[0])
+            nbytes = T * (rc_.Hq + 2 * rc_.Hkv) * rc_.d * 2 * 2 + T * 12
+            rope[key] = {"tokens": T, "heads": [rc_.Hq, rc_.Hkv], "d": rc_.d, "us": ms * 1e3,
+                         "us_warm": ms_warm * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                         "frac_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+                         "bytes": nbytes, "calls": calls}
+            del rq, rk, rv, rsid, rpos, rbt
+            if key != "rope_decode_step":
+                del rkc, rvc
+
     if rank != 0:
         return 0
     cpu = None if args.no_cpu_baseline else cpu_baseline_leg()
@@ -382,6 +435,14 @@ def run_gpu(args):
                      "traffic": load_traffic("norm.cu", "add_rms_norm_16384x8192")}
     else:
         line_norm = None
+    if rope is not None:
+        big = rope["rope_prefill_16k"]
+        line_rope = {"kernel": "rope_cache_kernel", "bound": "hbm", "achieved": big["gbs"],
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": big["gbs"] / peaks["hbm"],
+                     "peak_kind": "HBM copy (%s)" % peaks["src"], "workload": "rope_prefill_16k",
+                     "traffic": load_traffic("rope.cu", "rope_cache_write_prefill_16k")}
+    else:
+        line_rope = None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -400,6 +461,7 @@ def run_gpu(args):
                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
                      "peak_kind": "bf16 burst (%s)" % peaks["src"], "traffic": traffic},
         "roofline_norm": line_norm,
+        "roofline_rope": line_rope,
         "roofline_decode": {"kernel": "decode_split_kernel<128> + decode_combine_kernel<128>",
                             "bound": "hbm", "achieved": decode_bytes / (dec_avg_ms * 1e-3) / 1e9,
                             "peak": peaks["hbm"], "unit": "GB/s",
@@ -408,6 +470,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "add_rms_norm": norm,
+        "rope_cache_write": rope,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
@@ -423,6 +486,8 @@ def main():
     ap.add_argument("--impl", default="exattn", choices=["exattn", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope-calls", type=int, default=200,
+                    help="attn_rope_cache_write calls for the decode step (0 skips it)")
     ap.add_argument("--norm-calls", type=int, default=200,
                     help="add_rms_norm calls per shape (0 skips that measurement)")
     ap.add_argument("--ref-rows-total", type=int, default=60000,

@@ -342,6 +342,54 @@ int attn_add_rms_norm(const void* x, const void* residual, const void* weight, v
   return EXATTN_OK;
 }
 
+int attn_rope_cache_write(void* q, const void* k, const void* v, const int32_t* seq_ids,
+                          const int32_t* positions, const int32_t* block_table, void* k_cache,
+                          void* v_cache, int num_tokens, int Hq, int Hkv, int d, int num_seqs,
+                          int num_blocks, int max_blocks_per_seq, float base, void* stream) {
+  if (num_tokens < 0 || Hq < 1 || Hkv < 1 || num_seqs < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
+    return EXATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(base) || !(base > 1.f)) return EXATTN_ERR_INVALID_ARG;
+  if (d < 16 || d > exattn::kRopeMaxDim || d % 16 != 0) return EXATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * Hkv * 16 * d > (1ll << 40)) return EXATTN_ERR_UNSUPPORTED;
+  // at most 2048 work items (8 rotated pairs or one 16-byte copy) per token
+  if ((static_cast<long long>(Hq) + Hkv) * (d / 16) + static_cast<long long>(Hkv) * (d / 8) > 2048)
+    return EXATTN_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return EXATTN_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || seq_ids == nullptr || positions == nullptr ||
+      block_table == nullptr || k_cache == nullptr || v_cache == nullptr || k_cache == v_cache)
+    return EXATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(seq_ids) & 3u) || (reinterpret_cast<uintptr_t>(positions) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u))
+    return EXATTN_ERR_ALIGNMENT;
+  exattn::RopeArgs a;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    const int rc = device_state(&dev, &a.status);
+    if (rc != EXATTN_OK) return rc;
+  }
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.seq_ids = seq_ids;
+  a.positions = positions;
+  a.block_table = block_table;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_tokens = num_tokens;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.num_seqs = num_seqs;
+  a.num_blocks = num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_base = std::log2(static_cast<double>(base));
+  if (exattn::launch_rope_cache_write(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXATTN_ERR_CUDA;
+  return EXATTN_OK;
+}
+
 int attn_get_device_status(void* stream, unsigned int* status_out) {
   if (status_out == nullptr) return EXATTN_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;

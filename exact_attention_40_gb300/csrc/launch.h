@@ -65,4 +65,23 @@ constexpr int kNormMaxHidden = 16384;
 
 cudaError_t launch_add_rms_norm(const NormArgs& a, cudaStream_t stream);
 
+constexpr int kRopeMaxDim = 256;
+
+struct RopeArgs {
+  void* q;                    // [num_tokens, Hq, d] bf16, rotated in place
+  const void* k;              // [num_tokens, Hkv, d] bf16
+  const void* v;              // [num_tokens, Hkv, d] bf16
+  const int32_t* seq_ids;     // [num_tokens]
+  const int32_t* positions;   // [num_tokens]
+  const int32_t* block_table; // [num_seqs, max_blocks_per_seq]
+  void* k_cache;              // [num_blocks, Hkv, 16, d] bf16
+  void* v_cache;
+  unsigned int* status;       // device status word
+  long long num_tokens;
+  int Hq, Hkv, d, num_seqs, num_blocks, max_blocks_per_seq;
+  double log2_base;
+};
+
+cudaError_t launch_rope_cache_write(const RopeArgs& a, cudaStream_t stream);
+
 }  // namespace exattn

@@ -51,6 +51,9 @@ lib.attn_debug_expire_wait.argtypes = [ctypes.c_ulonglong, _P]
 lib.attn_debug_expire_wait.restype = _I
 lib.attn_add_rms_norm.argtypes = [_P, _P, _P, _P, _P, _I, _I, _F, _P]
 lib.attn_add_rms_norm.restype = _I
+lib.attn_rope_cache_write.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                      _F, _P]
+lib.attn_rope_cache_write.restype = _I
 lib.attn_shutdown.argtypes = []
 lib.attn_shutdown.restype = None
 
@@ -200,6 +203,38 @@ def attn_add_rms_norm(x, residual, weight, eps: float = 1e-6, out=None, residual
     if rc != EXATTN_OK:
         raise ExattnError("attn_add_rms_norm", rc)
     return out, residual_out
+
+
+def attn_rope_cache_write(q, k, v, seq_ids, positions, block_table, k_cache, v_cache,
+                          base: float = 500000.0, stream=None):
+    """Rotary embedding of q (in place) and k at each token's position, then
+    the rotated k and v stored into the paged caches.  q [T,Hq,d], k/v
+    [T,Hkv,d] bf16; seq_ids, positions int32 [T]; block_table int32
+    [S,max_blocks]; caches [num_blocks,Hkv,16,d] bf16.  Returns q."""
+    import torch
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("k", k, torch.bfloat16, 3)
+    _check_tensor("v", v, torch.bfloat16, 3)
+    _check_tensor("seq_ids", seq_ids, torch.int32, 1)
+    _check_tensor("positions", positions, torch.int32, 1)
+    _check_tensor("block_table", block_table, torch.int32, 2)
+    _check_tensor("k_cache", k_cache, torch.bfloat16, 4)
+    _check_tensor("v_cache", v_cache, torch.bfloat16, 4)
+    T, Hq, d = q.shape
+    num_blocks, Hkv, bs, dk = k_cache.shape
+    if tuple(k.shape) != (T, Hkv, d) or tuple(v.shape) != (T, Hkv, d) or dk != d or bs != 16 \
+            or tuple(v_cache.shape) != tuple(k_cache.shape) or seq_ids.shape[0] != T \
+            or positions.shape[0] != T:
+        raise ValueError("shape mismatch")
+    S, max_blocks = block_table.shape
+    with torch.cuda.device(q.device):
+        rc = lib.attn_rope_cache_write(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_ids.data_ptr(),
+                                       positions.data_ptr(), block_table.data_ptr(),
+                                       k_cache.data_ptr(), v_cache.data_ptr(), T, Hq, Hkv, d, S,
+                                       num_blocks, max_blocks, float(base), _stream_handle(stream))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_rope_cache_write", rc)
+    return q
 
 
 def attn_get_device_status(stream=None) -> int:

@@ -312,3 +312,51 @@ def norm_inputs_shape(seed: int, rows: int, hidden: int):
 
 def norm_inputs(cfg: NormConfig):
     return norm_inputs_shape(cfg.seed, cfg.rows, cfg.hidden)
+
+
+# ------------------------------------------------- RoPE + paged KV-cache write
+@dataclass(frozen=True)
+class RopeConfig:
+    name: str
+    ctx_lo: int      # context length of each sequence after the write
+    ctx_hi: int
+    num_seqs: int
+    new_tokens: int  # the last new_tokens positions of each sequence are written
+    Hq: int
+    Hkv: int
+    d: int
+    seed: int
+    base: float = 500000.0  # Llama-3's rotary base
+
+
+# One decode step of the paged-decode workload (one new token per sequence,
+# at position ctx_len - 1) and a 16384-token prefill chunk (64 sequences x
+# 256 tokens at positions 0 .. 255) of the same Llama-3-8B head layout.
+ROPE = {
+    "rope_decode_step": RopeConfig("rope_decode_step", 512, 8192, 64, 1, 32, 8, 128, 5),
+    "rope_prefill_16k": RopeConfig("rope_prefill_16k", 256, 256, 64, 256, 32, 8, 128, 8),
+}
+
+
+def rope_inputs_lens(seed: int, ctx_lens, new_tokens: int, Hq: int, Hkv: int, d: int):
+    """New tokens (the last new_tokens positions of each sequence, sequence by
+    sequence) with q [T,Hq,d], k, v [T,Hkv,d] ~ N(0,1) bf16, their seq_ids and
+    positions (int32 [T]), and the block table of the sequences' contexts.
+
+    Returns dict(q, k, v, seq_ids, positions, block_table, num_blocks)."""
+    ctx_lens = np.asarray(ctx_lens, np.int32)
+    table, nb = paged_layout(ctx_lens, 16, seed)
+    seq_ids, positions = [], []
+    for s, n in enumerate(ctx_lens):
+        first = max(0, int(n) - new_tokens)
+        positions.extend(range(first, int(n)))
+        seq_ids.extend([s] * (int(n) - first))
+    T = len(positions)
+    return dict(q=normal_bf16(seed, 0, (T, Hq, d)), k=normal_bf16(seed, 1, (T, Hkv, d)),
+                v=normal_bf16(seed, 2, (T, Hkv, d)), seq_ids=np.asarray(seq_ids, np.int32),
+                positions=np.asarray(positions, np.int32), block_table=table, num_blocks=nb)
+
+
+def rope_inputs(cfg: RopeConfig):
+    lens = ctx_lengths(cfg.seed, cfg.num_seqs, cfg.ctx_lo, cfg.ctx_hi)
+    return rope_inputs_lens(cfg.seed, lens, cfg.new_tokens, cfg.Hq, cfg.Hkv, cfg.d)

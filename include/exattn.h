@@ -176,6 +176,40 @@ int attn_add_rms_norm(const void* x, const void* residual, const void* weight, v
                       void* residual_out, int n_rows, int hidden, float eps, void* stream);
 
 /*
+ * Rotary position embedding of the new tokens' queries and keys, then the
+ * store of each token's rotated key and its value into the block-paged
+ * cache, in one kernel ("Inference Engineering VII.07: Kernel and Operator
+ * Fusion" page, section 2, "rope + cache write: RoPE then KV store";
+ * "Fused Kernel Compiler" page, table of fusion patterns, "RoPE
+ * embedding: sin, cos, rotate").  Pairs (i, i + d/2) of every head vector
+ * of token t turn by theta_i = positions[t] * base^(-2i/d):
+ *   y_i = x_i cos theta_i - x_(i+d/2) sin theta_i
+ *   y_(i+d/2) = x_(i+d/2) cos theta_i + x_i sin theta_i
+ * (angles reduced in fp64, rotation in fp32, one bf16 rounding).
+ *   q        [num_tokens, Hq, d] bf16: rotated in place
+ *   k, v     [num_tokens, Hkv, d] bf16: read only
+ *   seq_ids, positions int32 [num_tokens]: sequence and 0-based position of
+ *            each token
+ *   block_table int32 [num_seqs, max_blocks_per_seq] (as attn_decode_paged)
+ *   k_cache, v_cache [num_blocks, Hkv, 16, d] bf16: token t's rotated key
+ *            and its value go to slot positions[t] % 16 of physical block
+ *            block_table[seq][positions[t] / 16]; nothing else is written.
+ * d a multiple of 16 in [16, 256], (Hq + 3 Hkv) * d / 16 <= 2048 (e.g. up to
+ * 128 query and 32 key/value heads at d = 128); base finite and > 1; num_seqs,
+ * num_blocks, max_blocks_per_seq >= 1; num_tokens >= 0 (0 launches
+ * nothing).  q, k, v and the caches 16-byte aligned, the int32 arrays
+ * 4-byte aligned; k_cache != v_cache; no other overlap.  Two tokens that
+ * map to the same slot race.  A token whose sequence, position or table
+ * entry lies outside the table or the cache is rotated in q but stores
+ * nothing, and sets EXATTN_DEVICE_BOUNDS_BIT.  One kernel launch on
+ * `stream`, asynchronous.
+ */
+int attn_rope_cache_write(void* q, const void* k, const void* v, const int32_t* seq_ids,
+                          const int32_t* positions, const int32_t* block_table, void* k_cache,
+                          void* v_cache, int num_tokens, int Hq, int Hkv, int d, int num_seqs,
+                          int num_blocks, int max_blocks_per_seq, float base, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the status word of the
  * current device: 0, or an OR of EXATTN_DEVICE_*_BIT.  Returns EXATTN_OK
  * or EXATTN_ERR_CUDA.

@@ -149,3 +149,34 @@ def test_add_rms_norm_rejections(lib):
     assert norm(lib, out=FAKE + 50) == 3
     # nothing to do: success without touching the (null) pointers
     assert norm(lib, rows=0, x=None, r=None, w=None, out=None, h=None) == 0
+
+
+def rope(lib, q=FAKE, k=FAKE + 16, v=FAKE + 32, sid=FAKE + 48, pos=FAKE + 64, bt=FAKE + 80,
+         kc=FAKE + 96, vc=FAKE + 112, T=4, Hq=8, Hkv=2, d=128, S=2, nb=10, mb=4, base=500000.0):
+    return lib.lib.attn_rope_cache_write(q, k, v, sid, pos, bt, kc, vc, T, Hq, Hkv, d, S, nb, mb,
+                                         base, None)
+
+
+def test_rope_cache_write_rejections(lib):
+    assert rope(lib, d=24) == 2
+    assert rope(lib, d=272) == 2
+    assert rope(lib, d=8) == 2
+    assert rope(lib, T=-1) == 1
+    assert rope(lib, Hkv=0) == 1
+    assert rope(lib, S=0) == 1
+    assert rope(lib, nb=0) == 1
+    assert rope(lib, mb=0) == 1
+    assert rope(lib, base=1.0) == 1
+    assert rope(lib, base=float("nan")) == 1
+    assert rope(lib, q=None) == 1
+    assert rope(lib, bt=None) == 1
+    assert rope(lib, kc=FAKE + 96, vc=FAKE + 96) == 1
+    assert rope(lib, k=FAKE + 8) == 3
+    assert rope(lib, pos=FAKE + 2) == 3
+    assert rope(lib, T=0, q=None, k=None, v=None, sid=None, pos=None, bt=None, kc=None, vc=None) == 0
+
+
+def test_rope_cache_write_head_limit(lib):
+    # (Hq + 3 Hkv) * d / 16 <= 2048 work items per token
+    assert rope(lib, Hq=1024, Hkv=8, d=128) == 2
+    assert rope(lib, Hq=8, Hkv=1024, d=16) == 2
