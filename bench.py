@@ -292,6 +292,66 @@ def run_gpu(args):
     dec_avg_ms = dec_total / args.steps
     achieved = prefill_flops / (pre_avg_ms * 1e-3) / 1e12
 
+    # ---- the decode step replayed from a captured CUDA graph (same kernels,
+    # same buffers), L2 flushed before every replay, apart from the step
+    dgraph = None
+    if args.graph_steps > 0:
+        g, _, _ = exattn.attn_decode_graph_capture(dq, dk, dv, dbt, dcl, out=dout, lse=dlse,
+                                                   workspace=ws)
+        with g:
+            for _ in range(3):
+                g.launch()
+            torch.cuda.synchronize()
+            gevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.graph_steps)]
+            for e0, e1 in gevs:
+                flush.fill_(1)
+                e0.record(stream)
+                g.launch()
+                e1.record(stream)
+            torch.cuda.synchronize()
+        if exattn.attn_get_device_status() != 0:
+            raise RuntimeError("device status word set by the decode graph")
+        g_ms = sum(e0.elapsed_time(e1) for e0, e1 in gevs) / args.graph_steps
+        dgraph = {"us": g_ms * 1e3, "us_direct": dec_avg_ms * 1e3,
+                  "gbs": decode_bytes / (g_ms * 1e-3) / 1e9,
+                  "frac_hbm_peak": decode_bytes / (g_ms * 1e-3) / 1e9 / peaks["hbm"],
+                  "steps": args.graph_steps}
+        # a launch-bound decode (8 sequences x 512 tokens, ~1% of the
+        # workload's bytes): steps back to back, direct calls vs replays
+        sinp = synth.decode_inputs_lens(dc.seed, np.full(8, 512, np.int32), dc.Hq, dc.Hkv, dc.d,
+                                        nan_tail=False)
+        sq, skc, svc = to_dev(sinp["q"]), to_dev(sinp["k_cache"]), to_dev(sinp["v_cache"])
+        sbt, scl = to_dev(sinp["block_table"]), to_dev(sinp["ctx_lens"])
+        sout = torch.empty_like(sq)
+        slse = torch.empty((8, dc.Hq), device=dev, dtype=torch.float32)
+        sws = torch.empty(exattn.attn_decode_workspace_bytes(8, dc.Hq, dc.d, sinp["block_table"].shape[1]),
+                          device=dev, dtype=torch.uint8)
+        n_small = args.graph_steps
+        sg, _, _ = exattn.attn_decode_graph_capture(sq, skc, svc, sbt, scl, out=sout, lse=slse,
+                                                    workspace=sws)
+        with sg:
+            times = {}
+            for mode in ("direct", "graph", "direct", "graph"):
+                for _ in range(5):
+                    if mode == "graph":
+                        sg.launch()
+                    else:
+                        exattn.attn_decode_paged(sq, skc, svc, sbt, scl, out=sout, lse=slse, workspace=sws)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(n_small):
+                    if mode == "graph":
+                        sg.launch()
+                    else:
+                        exattn.attn_decode_paged(sq, skc, svc, sbt, scl, out=sout, lse=slse, workspace=sws)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times[mode] = min(times.get(mode, 1e30), e0.elapsed_time(e1) / n_small)
+        dgraph["small_8x512"] = {"us_direct": times["direct"] * 1e3, "us_graph": times["graph"] * 1e3,
+                                 "steps_back_to_back": n_small}
+
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if args.e2e_steps > 0:
@@ -471,6 +531,7 @@ def run_gpu(args):
         "e2e": e2e,
         "add_rms_norm": norm,
         "rope_cache_write": rope,
+        "decode_graph": dgraph,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
@@ -486,6 +547,8 @@ def main():
     ap.add_argument("--impl", default="exattn", choices=["exattn", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-steps", type=int, default=200,
+                    help="decode steps replayed from a captured CUDA graph (0 skips it)")
     ap.add_argument("--rope-calls", type=int, default=200,
                     help="attn_rope_cache_write calls for the decode step (0 skips it)")
     ap.add_argument("--norm-calls", type=int, default=200,

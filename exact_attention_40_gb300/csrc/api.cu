@@ -223,11 +223,15 @@ size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_p
   return o_bytes + lse_bytes;
 }
 
-int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
-                      const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
-                      int num_seqs, int Hq, int Hkv, int d, int block_size, int num_blocks,
-                      int max_blocks_per_seq, float scale, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host-side checks of attn_decode_paged's arguments (no CUDA call).
+int decode_validate(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
+                    int num_seqs, int Hq, int Hkv, int d, int block_size, int num_blocks,
+                    int max_blocks_per_seq, float scale, void* workspace, size_t workspace_bytes) {
   if (num_seqs < 0 || Hq < 1 || Hkv < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
     return EXATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !good_scale(scale)) return EXATTN_ERR_INVALID_ARG;
@@ -248,6 +252,23 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
   const size_t need = attn_decode_workspace_bytes(num_seqs, Hq, d, max_blocks_per_seq, block_size);
   if (workspace == nullptr || workspace_bytes < need) return EXATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return EXATTN_ERR_ALIGNMENT;
+  return EXATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
+                      int num_seqs, int Hq, int Hkv, int d, int block_size, int num_blocks,
+                      int max_blocks_per_seq, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  const int vrc = decode_validate(q, k_cache, v_cache, block_table, ctx_lens, out, lse, num_seqs, Hq, Hkv,
+                                  d, block_size, num_blocks, max_blocks_per_seq, scale, workspace,
+                                  workspace_bytes);
+  if (vrc != EXATTN_OK || num_seqs == 0) return vrc;
+  const long long cache_rows = static_cast<long long>(num_blocks) * Hkv * block_size;
 
   exattn::DecodeArgs a;
   exattn::DeviceGuard g;
@@ -286,6 +307,73 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
       return EXATTN_ERR_CUDA;
   }
   return EXATTN_OK;
+}
+
+}  // extern "C"
+
+struct exattn_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+int attn_decode_graph_capture(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, const int32_t* ctx_lens, void* out,
+                              float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
+                              int num_blocks, int max_blocks_per_seq, float scale, void* workspace,
+                              size_t workspace_bytes, exattn_graph** graph_out) {
+  if (graph_out == nullptr) return EXATTN_ERR_INVALID_ARG;
+  *graph_out = nullptr;
+  if (num_seqs < 1) return EXATTN_ERR_INVALID_ARG;
+  const int vrc = decode_validate(q, k_cache, v_cache, block_table, ctx_lens, out, lse, num_seqs, Hq, Hkv,
+                                  d, block_size, num_blocks, max_blocks_per_seq, scale, workspace,
+                                  workspace_bytes);
+  if (vrc != EXATTN_OK) return vrc;
+  {
+    // the status word's address is looked up outside the capture
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    unsigned int* status;
+    const int rc = device_state(&dev, &status);
+    if (rc != EXATTN_OK) return rc;
+  }
+  cudaStream_t cs;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return EXATTN_ERR_CUDA;
+  }
+  const int rc = attn_decode_paged(q, k_cache, v_cache, block_table, ctx_lens, out, lse, num_seqs, Hq,
+                                   Hkv, d, block_size, num_blocks, max_blocks_per_seq, scale, workspace,
+                                   workspace_bytes, cs);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(cs, &graph);
+  cudaStreamDestroy(cs);
+  if (rc != EXATTN_OK || e != cudaSuccess) {
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    return rc != EXATTN_OK ? rc : EXATTN_ERR_CUDA;
+  }
+  cudaGraphExec_t exec;
+  if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return EXATTN_ERR_CUDA;
+  }
+  *graph_out = new exattn_graph{graph, exec};
+  return EXATTN_OK;
+}
+
+int attn_graph_launch(exattn_graph* graph, void* stream) {
+  if (graph == nullptr) return EXATTN_ERR_INVALID_ARG;
+  return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? EXATTN_OK
+                                                                                          : EXATTN_ERR_CUDA;
+}
+
+int attn_graph_destroy(exattn_graph* graph) {
+  if (graph == nullptr) return EXATTN_OK;
+  const bool ok = cudaGraphExecDestroy(graph->exec) == cudaSuccess && cudaGraphDestroy(graph->graph) == cudaSuccess;
+  delete graph;
+  return ok ? EXATTN_OK : EXATTN_ERR_CUDA;
 }
 
 int attn_decode_paged_static(const void* q, const void* k_cache, const void* v_cache,

@@ -54,6 +54,13 @@ lib.attn_add_rms_norm.restype = _I
 lib.attn_rope_cache_write.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                       _F, _P]
 lib.attn_rope_cache_write.restype = _I
+lib.attn_decode_graph_capture.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                          _P, _SZ, ctypes.POINTER(ctypes.c_void_p)]
+lib.attn_decode_graph_capture.restype = _I
+lib.attn_graph_launch.argtypes = [_P, _P]
+lib.attn_graph_launch.restype = _I
+lib.attn_graph_destroy.argtypes = [_P]
+lib.attn_graph_destroy.restype = _I
 lib.attn_shutdown.argtypes = []
 lib.attn_shutdown.restype = None
 
@@ -235,6 +242,78 @@ def attn_rope_cache_write(q, k, v, seq_ids, positions, block_table, k_cache, v_c
     if rc != EXATTN_OK:
         raise ExattnError("attn_rope_cache_write", rc)
     return q
+
+
+class DecodeGraph:
+    """A captured decode step (split kernel + merge).  It holds references to
+    the tensors it was captured with; change their contents in place and
+    call launch() to replay.  close() frees it (no replay may be pending)."""
+
+    def __init__(self, handle, tensors):
+        self._h = handle
+        self._tensors = tensors
+
+    def launch(self, stream=None):
+        if self._h is None:
+            raise ValueError("graph already closed")
+        rc = lib.attn_graph_launch(self._h, _stream_handle(stream))
+        if rc != EXATTN_OK:
+            raise ExattnError("attn_graph_launch", rc)
+
+    def close(self):
+        if self._h is not None:
+            rc = lib.attn_graph_destroy(self._h)
+            self._h = None
+            self._tensors = None
+            if rc != EXATTN_OK:
+                raise ExattnError("attn_graph_destroy", rc)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def attn_decode_graph_capture(q, k_cache, v_cache, block_table, ctx_lens, scale: float | None = None,
+                              out=None, lse=None, workspace=None, return_lse: bool = True):
+    """Capture one attn_decode_paged step (same arguments) into a CUDA graph.
+
+    Returns (DecodeGraph, out, lse); nothing runs until graph.launch()."""
+    import torch
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("k_cache", k_cache, torch.bfloat16, 4)
+    _check_tensor("v_cache", v_cache, torch.bfloat16, 4)
+    _check_tensor("block_table", block_table, torch.int32, 2)
+    _check_tensor("ctx_lens", ctx_lens, torch.int32, 1)
+    S, Hq, d = q.shape
+    num_blocks, Hkv, bs, dk = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or dk != d or block_table.shape[0] != S \
+            or ctx_lens.shape[0] != S:
+        raise ValueError("shape mismatch")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((S, Hq), device=q.device, dtype=torch.float32)
+    need = attn_decode_workspace_bytes(S, Hq, d, max_blocks, bs)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    h = ctypes.c_void_p()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_decode_graph_capture(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                           block_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
+                                           lse.data_ptr() if lse is not None else None, S, Hq, Hkv, d,
+                                           bs, num_blocks, max_blocks, float(scale),
+                                           workspace.data_ptr(),
+                                           workspace.numel() * workspace.element_size(),
+                                           ctypes.byref(h))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_decode_graph_capture", rc)
+    g = DecodeGraph(h, (q, k_cache, v_cache, block_table, ctx_lens, out, lse, workspace))
+    return g, out, lse
 
 
 def attn_get_device_status(stream=None) -> int:

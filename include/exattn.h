@@ -176,6 +176,33 @@ int attn_add_rms_norm(const void* x, const void* residual, const void* weight, v
                       void* residual_out, int n_rows, int hidden, float eps, void* stream);
 
 /*
+ * CUDA-graph capture of one decode step ("Optimizing LLM Inference ..."
+ * page, section Compilation and CUDA Graphs: a captured sequence of
+ * launches is replayed with one call, removing per-launch overhead).
+ * attn_decode_graph_capture records exactly the work attn_decode_paged
+ * would enqueue for these arguments (split kernel + merge) on a private
+ * stream and instantiates it; nothing runs.  The graph keeps every pointer
+ * and size it was captured with: the caller keeps those buffers alive and
+ * may change their contents (q, ctx_lens, block_table, the caches) between
+ * launches; ctx_lens entries must stay <= max_blocks_per_seq * 16.  Same
+ * argument rules and errors as attn_decode_paged, plus num_seqs >= 1 and a
+ * non-NULL graph_out (set to NULL on failure).  The graph belongs to the
+ * device current at capture.
+ * attn_graph_launch enqueues one replay on `stream` (asynchronous).
+ * attn_graph_destroy frees the graph (NULL is a no-op); no replay may still
+ * be pending.
+ */
+typedef struct exattn_graph exattn_graph;
+
+int attn_decode_graph_capture(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, const int32_t* ctx_lens, void* out,
+                              float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
+                              int num_blocks, int max_blocks_per_seq, float scale, void* workspace,
+                              size_t workspace_bytes, exattn_graph** graph_out);
+int attn_graph_launch(exattn_graph* graph, void* stream);
+int attn_graph_destroy(exattn_graph* graph);
+
+/*
  * Rotary position embedding of the new tokens' queries and keys, then the
  * store of each token's rotated key and its value into the block-paged
  * cache, in one kernel ("Inference Engineering VII.07: Kernel and Operator

@@ -180,3 +180,18 @@ def test_rope_cache_write_head_limit(lib):
     # (Hq + 3 Hkv) * d / 16 <= 2048 work items per token
     assert rope(lib, Hq=1024, Hkv=8, d=128) == 2
     assert rope(lib, Hq=8, Hkv=1024, d=16) == 2
+
+
+def test_graph_calls_validate_on_the_host(lib):
+    h = ctypes.c_void_p()
+    so = lib.lib
+    # bad arguments are rejected before any capture starts
+    assert so.attn_decode_graph_capture(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 32, 10,
+                                        4, 0.1, FAKE, 1 << 20, ctypes.byref(h)) in (1, 2)
+    assert so.attn_decode_graph_capture(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 8, 2, 128, 16, 10,
+                                        4, 0.1, FAKE, 1 << 20, ctypes.byref(h)) == 1
+    assert so.attn_decode_graph_capture(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 16, 10,
+                                        4, 0.1, FAKE, 1 << 20, None) == 1
+    assert not h.value
+    assert so.attn_graph_launch(None, None) == 1
+    assert so.attn_graph_destroy(None) == 0
