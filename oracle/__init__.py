@@ -61,6 +61,8 @@ def _load():
     lib.oracle_add_rms_norm_f64.restype = I
     lib.oracle_rope_cache_write_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D, P, P, P]
     lib.oracle_rope_cache_write_f64.restype = I
+    lib.oracle_attn_bwd_f64.argtypes = [P, P, P, P, I, I, I, L, L, I, D, I, P, P, P]
+    lib.oracle_attn_bwd_f64.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     lib.oracle_set_num_threads.argtypes = [I]
@@ -203,3 +205,21 @@ def rope_cache_write(q, k, seq_ids, positions, block_table, num_blocks: int, bas
     if rc != 0:
         raise ValueError("oracle_rope_cache_write_f64 rejected its arguments")
     return q_out, k_out, slot
+
+
+def attn_bwd(q, k, v, dout, scale: float, causal: bool):
+    """Gradients of attention.  q, dout [B,Hq,Nq,d], k/v [B,Hkv,Nk,d] (uint16
+    bf16 bits).  Returns (dq [B,Hq,Nq,d], dk, dv [B,Hkv,Nk,d]) in fp64."""
+    q, k, v, dout = _u16(q), _u16(k), _u16(v), _u16(dout)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk_ = k.shape
+    if k.shape != v.shape or Bk != B or dk_ != d or dout.shape != q.shape:
+        raise ValueError("shape mismatch")
+    dq = np.zeros(q.shape, np.float64)
+    dk = np.zeros(k.shape, np.float64)
+    dv = np.zeros(k.shape, np.float64)
+    rc = _load().oracle_attn_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, Hq, Hkv, Nq, Nk, d,
+                                     float(scale), int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_f64 rejected its arguments")
+    return dq, dk, dv

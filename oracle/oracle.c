@@ -371,3 +371,88 @@ int oracle_rope_cache_write_f64(const uint16_t* q, const uint16_t* k, const int3
   }
   return 0;
 }
+
+/* Gradients of scaled dot-product attention with respect to Q, K and V,
+ * given the gradient dO of the output ("Kernel Fusion, Softmax, and
+ * Attention" page: training runs a different schedule of the same
+ * attention equation; the chain rule through O = P V and P = softmax(S)):
+ *
+ *   P_ij  = exp(s_ij - lse_i)           the forward's probabilities
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = <dO_i, v_j>
+ *   D_i   = sum_j P_ij dP_ij
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale sum_j dS_ij k_j
+ *   dK_j  = scale sum_i dS_ij q_i
+ *
+ * with the forward's mask, and dK, dV of a key/value head summed over the
+ * query heads that read it.  q, dout [B, Hq, Nq, d], k, v [B, Hkv, Nk, d]
+ * bf16 bits; dq [B, Hq, Nq, d], dk, dv [B, Hkv, Nk, d] fp64.  The full
+ * probability row of each query is formed in fp64; a row that sees no key
+ * contributes nothing.  Returns nonzero for a bad argument. */
+int oracle_attn_bwd_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                        int B, int Hq, int Hkv, long Nq, long Nk, int d, double scale, int causal,
+                        double* dq, double* dk, double* dv) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || d < 1) return 1;
+  const int G = Hq / Hkv;
+  long bk;
+#pragma omp parallel for schedule(dynamic)
+  for (bk = 0; bk < (long)B * Hkv; ++bk) {
+    const long b = bk / Hkv, hk = bk % Hkv;
+    const uint16_t* kh = k + (size_t)bk * Nk * d;
+    const uint16_t* vh = v + (size_t)bk * Nk * d;
+    double* dkh = dk + (size_t)bk * Nk * d;
+    double* dvh = dv + (size_t)bk * Nk * d;
+    for (size_t e = 0; e < (size_t)Nk * d; ++e) dkh[e] = dvh[e] = 0.0;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+    double* dp = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+    double* gd = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int g = 0; g < G; ++g) {
+      const long hq = hk * G + g;
+      const size_t head = (size_t)(b * Hq + hq) * Nq * d;
+      for (long i = 0; i < Nq; ++i) {
+        const long n_vis = visible_keys(i, Nq, Nk, causal);
+        double* dqi = dq + head + (size_t)i * d;
+        for (int t = 0; t < d; ++t) {
+          qd[t] = bf16_to_f64(q[head + (size_t)i * d + t]);
+          gd[t] = bf16_to_f64(dout[head + (size_t)i * d + t]);
+          dqi[t] = 0.0;
+        }
+        if (n_vis <= 0) continue;
+        double m = -INFINITY;
+        for (long j = 0; j < n_vis; ++j) {
+          double acc = 0.0;
+          for (int t = 0; t < d; ++t) acc += qd[t] * bf16_to_f64(kh[(size_t)j * d + t]);
+          s[j] = scale * acc;
+          if (s[j] > m) m = s[j];
+        }
+        double l = 0.0;
+        for (long j = 0; j < n_vis; ++j) l += exp(s[j] - m);
+        const double lse = m + log(l);
+        double D = 0.0;
+        for (long j = 0; j < n_vis; ++j) {
+          s[j] = exp(s[j] - lse); /* now P_ij */
+          double acc = 0.0;
+          for (int t = 0; t < d; ++t) acc += gd[t] * bf16_to_f64(vh[(size_t)j * d + t]);
+          dp[j] = acc;
+          D += s[j] * acc;
+        }
+        for (long j = 0; j < n_vis; ++j) {
+          const double pij = s[j];
+          const double ds = pij * (dp[j] - D);
+          for (int t = 0; t < d; ++t) {
+            dqi[t] += scale * ds * bf16_to_f64(kh[(size_t)j * d + t]);
+            dkh[(size_t)j * d + t] += scale * ds * qd[t];
+            dvh[(size_t)j * d + t] += pij * gd[t];
+          }
+        }
+      }
+    }
+    free(s);
+    free(dp);
+    free(qd);
+    free(gd);
+  }
+  return 0;
+}
