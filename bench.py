@@ -352,6 +352,37 @@ def run_gpu(args):
         dgraph["small_8x512"] = {"us_direct": times["direct"] * 1e3, "us_graph": times["graph"] * 1e3,
                                  "steps_back_to_back": n_small}
 
+    # ---- attention backward on the prefill workload (dO ~ N(0,1)), timed
+    # apart from the step; FLOPs = 2.5 x the forward's (the backward's five
+    # products: S again, dP, dV, dK, dQ), L2 flushed before every call
+    bwd = None
+    if args.bwd_calls > 0:
+        do_np = synth.normal_bf16(pc.seed, 3, tuple(q.shape))
+        dod = to_dev(do_np)
+        exattn.attn_fwd(q, k, v, causal=True, out=out, lse=lse)
+        bdq, bdk, bdv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(exattn.lib.attn_bwd_workspace_bytes(pc.B, pc.Hq, pc.Hkv, pc.N, pc.N, pc.d),
+                          device=dev, dtype=torch.uint8)
+        for _ in range(3):
+            exattn.attn_bwd(q, k, v, out, dod, lse, causal=True, dq=bdq, dk=bdk, dv=bdv, workspace=bws)
+        torch.cuda.synchronize()
+        bevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.bwd_calls)]
+        for e0, e1 in bevs:
+            flush.fill_(1)
+            e0.record(stream)
+            exattn.attn_bwd(q, k, v, out, dod, lse, causal=True, dq=bdq, dk=bdk, dv=bdv, workspace=bws)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if exattn.attn_get_device_status() != 0:
+            raise RuntimeError("device status word set by attn_bwd")
+        b_ms = sum(e0.elapsed_time(e1) for e0, e1 in bevs) / args.bwd_calls
+        b_flops = 2.5 * prefill_flops
+        bwd = {"workload": "llama3_8b_causal", "tflops": b_flops / (b_ms * 1e-3) / 1e12, "ms": b_ms,
+               "flops": b_flops, "frac_bf16_peak": b_flops / (b_ms * 1e-3) / 1e12 / peaks["bf16"],
+               "calls": args.bwd_calls, "kernels": "dsum + dK/dV + dQ (mma.sync)"}
+        del dod, bdq, bdk, bdv, bws
+
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if args.e2e_steps > 0:
@@ -532,6 +563,7 @@ def run_gpu(args):
         "add_rms_norm": norm,
         "rope_cache_write": rope,
         "decode_graph": dgraph,
+        "attn_bwd": bwd,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
@@ -547,6 +579,8 @@ def main():
     ap.add_argument("--impl", default="exattn", choices=["exattn", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-calls", type=int, default=50,
+                    help="attention backward calls on the prefill workload (0 skips it)")
     ap.add_argument("--graph-steps", type=int, default=200,
                     help="decode steps replayed from a captured CUDA graph (0 skips it)")
     ap.add_argument("--rope-calls", type=int, default=200,

@@ -478,6 +478,59 @@ int attn_rope_cache_write(void* q, const void* k, const void* v, const int32_t* 
   return EXATTN_OK;
 }
 
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128)) return 0;
+  const size_t dsum = (static_cast<size_t>(B) * Hq * Nq * sizeof(float) + 15) / 16 * 16;
+  // with query heads sharing a KV head: fp32 dK and dV partials per query head
+  const size_t part = Hq > Hkv ? static_cast<size_t>(B) * Hq * Nk * d * sizeof(float) * 2 : 0;
+  return dsum + part;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+             int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0) return EXATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !good_scale(scale)) return EXATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return EXATTN_ERR_UNSUPPORTED;
+  if (Nq > (1 << 30) || Nk > (1 << 30) || static_cast<long long>(B) * Hq > 65535 ||
+      static_cast<long long>(B) * Hkv > 65535)
+    return EXATTN_ERR_UNSUPPORTED;
+  if (B == 0 || (Nq == 0 && Nk == 0)) return EXATTN_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr ||
+      lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+    return EXATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
+    return EXATTN_ERR_ALIGNMENT;
+  const size_t need = attn_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return EXATTN_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(workspace)) return EXATTN_ERR_ALIGNMENT;
+  exattn::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.dsum = static_cast<float*>(workspace);
+  a.part = Hq > Hkv ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                               (static_cast<size_t>(B) * Hq * Nq * sizeof(float) + 15) / 16 * 16)
+                    : nullptr;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  if (exattn::launch_bwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;
+  return EXATTN_OK;
+}
+
 int attn_get_device_status(void* stream, unsigned int* status_out) {
   if (status_out == nullptr) return EXATTN_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;

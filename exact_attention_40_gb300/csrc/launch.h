@@ -84,4 +84,22 @@ struct RopeArgs {
 
 cudaError_t launch_rope_cache_write(const RopeArgs& a, cudaStream_t stream);
 
+struct BwdArgs {
+  const void* q;     // [B, Hq, Nq, d] bf16
+  const void* k;     // [B, Hkv, Nk, d] bf16
+  const void* v;
+  const void* out;   // forward output [B, Hq, Nq, d] bf16
+  const void* dout;  // [B, Hq, Nq, d] bf16
+  const float* lse;  // forward log-sum-exp [B, Hq, Nq]
+  float* dsum;       // workspace: D [B, Hq, Nq]
+  float* part;       // workspace (Hq > Hkv): dK, dV partials per query head, fp32
+  void* dq;          // [B, Hq, Nq, d] bf16
+  void* dk;          // [B, Hkv, Nk, d] bf16
+  void* dv;
+  int B, Hq, Hkv, Nq, Nk, d, causal;
+  float scale;
+};
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+
 }  // namespace exattn

@@ -61,6 +61,10 @@ lib.attn_graph_launch.argtypes = [_P, _P]
 lib.attn_graph_launch.restype = _I
 lib.attn_graph_destroy.argtypes = [_P]
 lib.attn_graph_destroy.restype = _I
+lib.attn_bwd_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I]
+lib.attn_bwd_workspace_bytes.restype = _SZ
+lib.attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]
+lib.attn_bwd.restype = _I
 lib.attn_shutdown.argtypes = []
 lib.attn_shutdown.restype = None
 
@@ -314,6 +318,37 @@ def attn_decode_graph_capture(q, k_cache, v_cache, block_table, ctx_lens, scale:
         raise ExattnError("attn_decode_graph_capture", rc)
     g = DecodeGraph(h, (q, k_cache, v_cache, block_table, ctx_lens, out, lse, workspace))
     return g, out, lse
+
+
+def attn_bwd(q, k, v, out, dout, lse, causal: bool = False, scale: float | None = None, dq=None,
+             dk=None, dv=None, workspace=None, stream=None):
+    """Attention backward.  q, out, dout [B,Hq,Nq,d], k/v [B,Hkv,Nk,d] bf16;
+    lse [B,Hq,Nq] fp32 from attn_fwd.  Returns (dq, dk, dv), bf16."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_tensor(name, t, torch.bfloat16, 4)
+    _check_tensor("lse", lse, torch.float32, 3)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk_ = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or dk_ != d or tuple(out.shape) != tuple(q.shape) \
+            or tuple(dout.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(lib.attn_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Nq,
+                          Nk, d, float(scale), int(bool(causal)), workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != EXATTN_OK:
+        raise ExattnError("attn_bwd", rc)
+    return dq, dk, dv
 
 
 def attn_get_device_status(stream=None) -> int:

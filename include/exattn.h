@@ -176,6 +176,36 @@ int attn_add_rms_norm(const void* x, const void* residual, const void* weight, v
                       void* residual_out, int n_rows, int hidden, float eps, void* stream);
 
 /*
+ * Bytes of caller-provided device workspace attn_bwd needs: D (fp32
+ * [B, Hq, Nq], rounded up to 16 bytes) and, when query heads share a KV head
+ * (Hq > Hkv), fp32 dK and dV partials per query head ([2][B*Hq][Nk][d]).
+ * Returns 0 for invalid arguments (or nothing to store).
+ */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+
+/*
+ * Attention backward: the gradients of attn_fwd's output with respect to
+ * q, k and v, given dout ("Kernel Fusion, Softmax, and Attention" page:
+ * training runs a different schedule of the same attention equation).  With
+ * P = softmax(scale * q k^T + mask) rebuilt from the forward's lse:
+ *   D_i  = <dout_i, out_i>,  dS = P * (dout v^T - D),
+ *   dv = P^T dout,  dk = scale dS^T q,  dq = scale dS k,
+ * dk, dv summed over the query heads of each KV head.
+ *   q, out, dout, dq [B, Hq, Nq, d] bf16;  k, v, dk, dv [B, Hkv, Nk, d] bf16
+ *   lse [B, Hq, Nq] fp32: attn_fwd's log-sum-exp for the same inputs
+ *   workspace: attn_bwd_workspace_bytes(...) bytes, 16-byte aligned (its
+ *   contents need not be initialised and are clobbered)
+ * scale, causal (same bottom-right mask), d and the head counts as attn_fwd;
+ * B*Hq, B*Hkv <= 65535.  All tensor pointers 16-byte aligned (lse 4); no
+ * output may overlap an input.  B == 0 or Nq == Nk == 0 launches nothing.
+ * Up to four kernel launches on `stream` (D, dk/dv, their sum over query
+ * heads when Hq > Hkv, dq); asynchronous, deterministic (no atomics).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+             int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * CUDA-graph capture of one decode step ("Optimizing LLM Inference ..."
  * page, section Compilation and CUDA Graphs: a captured sequence of
  * launches is replayed with one call, removing per-launch overhead).

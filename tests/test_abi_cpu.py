@@ -195,3 +195,29 @@ def test_graph_calls_validate_on_the_host(lib):
     assert not h.value
     assert so.attn_graph_launch(None, None) == 1
     assert so.attn_graph_destroy(None) == 0
+
+
+def bwd(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, do=FAKE, lse=FAKE, dq=FAKE + 16, dk=FAKE + 32,
+        dv=FAKE + 48, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=128, scale=0.1, causal=1, ws=FAKE + 64,
+        ws_bytes=1 << 20):
+    return lib.lib.attn_bwd(q, k, v, out, do, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, ws,
+                            ws_bytes, None)
+
+
+def test_bwd_rejections_and_workspace(lib):
+    assert lib.lib.attn_bwd_workspace_bytes(2, 4, 4, 10, 7, 64) == 2 * 4 * 10 * 4
+    assert lib.lib.attn_bwd_workspace_bytes(1, 1, 1, 3, 5, 128) == 16
+    # query heads sharing a KV head: fp32 dK, dV partials per query head
+    assert lib.lib.attn_bwd_workspace_bytes(1, 4, 2, 8, 6, 64) == 4 * 8 * 4 + 4 * 6 * 64 * 4 * 2
+    assert lib.lib.attn_bwd_workspace_bytes(1, 4, 3, 8, 6, 64) == 0
+    assert bwd(lib, d=96) == 2
+    assert bwd(lib, Hq=3, Hkv=2) == 1
+    assert bwd(lib, scale=-1.0) == 1
+    assert bwd(lib, lse=None) == 1
+    assert bwd(lib, dk=None) == 1
+    assert bwd(lib, dq=FAKE + 8) == 3
+    assert bwd(lib, lse=FAKE + 2) == 3
+    assert bwd(lib, ws=None) == 4
+    assert bwd(lib, ws_bytes=8) == 4
+    assert bwd(lib, B=70000) == 2
+    assert bwd(lib, B=0, q=None) == 0
