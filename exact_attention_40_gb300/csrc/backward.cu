@@ -80,26 +80,6 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const __nv_bfloat16* s
   }
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // A operand (16 rows x 16 k) from a row-major tile: rows r0.., k 16kk..
 template <int D>
 __device__ __forceinline__ void lda(uint32_t base, int r0, int kk, uint32_t (&a)[4]) {
@@ -256,10 +236,10 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
           uint32_t bq[4], bd[4];
           ldb_nk<D>(s_q[buf], c0 + 16 * np, kk, bq);
           ldb_nk<D>(s_do[buf], c0 + 16 * np, kk, bd);
-          mma16816(st[2 * np], ak, bq[0], bq[1]);
-          mma16816(st[2 * np + 1], ak, bq[2], bq[3]);
-          mma16816(dpt[2 * np], av, bd[0], bd[1]);
-          mma16816(dpt[2 * np + 1], av, bd[2], bd[3]);
+          mma_bf16_16816(st[2 * np], ak, bq[0], bq[1]);
+          mma_bf16_16816(st[2 * np + 1], ak, bq[2], bq[3]);
+          mma_bf16_16816(dpt[2 * np], av, bd[0], bd[1]);
+          mma_bf16_16816(dpt[2 * np + 1], av, bd[2], bd[3]);
         }
       }
 #pragma unroll
@@ -294,10 +274,10 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
           uint32_t bd[4], bq[4];
           ldb_kn<D>(s_do[buf], 16 * np, 2 * half + kk, bd);
           ldb_kn<D>(s_q[buf], 16 * np, 2 * half + kk, bq);
-          mma16816(dv[2 * np], pa[kk], bd[0], bd[1]);
-          mma16816(dv[2 * np + 1], pa[kk], bd[2], bd[3]);
-          mma16816(dk[2 * np], da[kk], bq[0], bq[1]);
-          mma16816(dk[2 * np + 1], da[kk], bq[2], bq[3]);
+          mma_bf16_16816(dv[2 * np], pa[kk], bd[0], bd[1]);
+          mma_bf16_16816(dv[2 * np + 1], pa[kk], bd[2], bd[3]);
+          mma_bf16_16816(dk[2 * np], da[kk], bq[0], bq[1]);
+          mma_bf16_16816(dk[2 * np + 1], da[kk], bq[2], bq[3]);
         }
     }
     __syncthreads();  // this buffer is refilled by the next prefetch
@@ -412,10 +392,10 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
         uint32_t bk_[4], bv[4];
         ldb_nk<D>(s_k[buf], 16 * np, kk, bk_);
         ldb_nk<D>(s_v[buf], 16 * np, kk, bv);
-        mma16816(s[2 * np], aq, bk_[0], bk_[1]);
-        mma16816(s[2 * np + 1], aq, bk_[2], bk_[3]);
-        mma16816(dp[2 * np], ad, bv[0], bv[1]);
-        mma16816(dp[2 * np + 1], ad, bv[2], bv[3]);
+        mma_bf16_16816(s[2 * np], aq, bk_[0], bk_[1]);
+        mma_bf16_16816(s[2 * np + 1], aq, bk_[2], bk_[3]);
+        mma_bf16_16816(dp[2 * np], ad, bv[0], bv[1]);
+        mma_bf16_16816(dp[2 * np + 1], ad, bv[2], bv[3]);
       }
     }
     const long long key0 = static_cast<long long>(kb) * kBwdRows;
@@ -438,8 +418,8 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
       for (int np = 0; np < D / 16; ++np) {
         uint32_t bk_[4];
         ldb_kn<D>(s_k[buf], 16 * np, kk, bk_);
-        mma16816(dq[2 * np], a[kk], bk_[0], bk_[1]);
-        mma16816(dq[2 * np + 1], a[kk], bk_[2], bk_[3]);
+        mma_bf16_16816(dq[2 * np], a[kk], bk_[0], bk_[1]);
+        mma_bf16_16816(dq[2 * np + 1], a[kk], bk_[2], bk_[3]);
       }
     __syncthreads();  // this buffer is refilled by the next prefetch
   }

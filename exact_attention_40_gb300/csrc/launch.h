@@ -8,6 +8,20 @@
 
 namespace exattn {
 
+// Streaming multiprocessors of the current device (cached per device; 0 on
+// error).  Grids of the persistent and grid-stride kernels are sized by it.
+inline int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // Wait budget for every bounded pipeline wait inside the kernels.
 struct DeviceGuard {
   unsigned int* status;        // device status word (OR of EXATTN_DEVICE_*_BIT)

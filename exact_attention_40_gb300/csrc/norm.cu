@@ -39,20 +39,6 @@ __device__ __forceinline__ void st_once(uint4* p, uint4 v) {
                : "memory");
 }
 
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
-}
-
 // VPT: 8-value vectors per thread per tensor; a row has nvec = hidden / 8
 // vectors, vector v of the row belongs to thread v % 256.
 template <int VPT>
@@ -83,8 +69,8 @@ __global__ void __launch_bounds__(kNormThreads) add_rms_norm_kernel(const NormAr
       const int v = threadIdx.x + i * kNormThreads;
       if (v < nvec) {
         float fx[8], fr[8];
-        unpack8(xv[i], fx);
-        unpack8(rv[i], fr);
+        unpack_bf16x8(xv[i], fx);
+        unpack_bf16x8(rv[i], fr);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           h[i][e] = fx[e] + fr[e];
@@ -105,34 +91,22 @@ __global__ void __launch_bounds__(kNormThreads) add_rms_norm_kernel(const NormAr
       const int v = threadIdx.x + i * kNormThreads;
       if (v < nvec) {
         float fw[8], o[8];
-        unpack8(__ldg(w + v), fw);
+        unpack_bf16x8(__ldg(w + v), fw);
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = h[i][e] * inv * fw[e];
-        st_once(out + base + v, pack8(o));
-        st_once(h_out + base + v, pack8(h[i]));
+        st_once(out + base + v, pack_bf16x8(o));
+        st_once(h_out + base + v, pack_bf16x8(h[i]));
       }
     }
     __syncthreads();  // warp_ss is refilled for the next row
   }
 }
 
-int norm_sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 }  // namespace
 
 cudaError_t launch_add_rms_norm(const NormArgs& a, cudaStream_t stream) {
   const int nvec = a.hidden / 8;
-  const int sms = norm_sm_count();
+  const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   // Eight 256-thread CTAs fit an SM; more rows than that are walked by a
   // grid-stride loop.

@@ -589,18 +589,6 @@ size_t smem_bytes_for() {
   return s < 120 * 1024 ? 120 * 1024 : s;
 }
 
-int sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 template <int D>
 cudaError_t launch_d(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t stream) {
   KernelParams kp;
@@ -620,7 +608,7 @@ cudaError_t launch_d(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t st
   kp.n_items = static_cast<int>(n_items);
   kp.causal = a.causal;
   kp.scale_log2 = a.scale * 1.4426950408889634f;
-  const int sms = sm_count();
+  const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const size_t smem = smem_bytes_for<D>();
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -33,32 +33,18 @@ namespace {
 
 constexpr int kRopeThreads = 256;
 
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
-}
-
 // Rotates the 8 pairs (lo[e], hi[e]) by angles with cosines c[e], sines s[e].
 __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float* c, const float* s) {
   float a[8], b[8], ya[8], yb[8];
-  unpack8(lo, a);
-  unpack8(hi, b);
+  unpack_bf16x8(lo, a);
+  unpack_bf16x8(hi, b);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     ya[e] = fmaf(a[e], c[e], -b[e] * s[e]);
     yb[e] = fmaf(b[e], c[e], a[e] * s[e]);
   }
-  lo = pack8(ya);
-  hi = pack8(yb);
+  lo = pack_bf16x8(ya);
+  hi = pack_bf16x8(yb);
 }
 
 // MAXI: work items per thread per token (q and k items are 8 pairs, v items
@@ -144,22 +130,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs
   }
 }
 
-int rope_sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 }  // namespace
 
 cudaError_t launch_rope_cache_write(const RopeArgs& a, cudaStream_t stream) {
-  const int sms = rope_sm_count();
+  const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const long long cap = static_cast<long long>(sms) * 8;
   const int grid = static_cast<int>(a.num_tokens < cap ? a.num_tokens : cap);
