@@ -21,7 +21,7 @@
  * softmax is the two-pass safe form, with no running (online) update.  The
  * fused kernels reach the same numbers up to rounding order.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *   - causal mask aligned bottom-right: query i sees keys j <= i + Nk - Nq;
  *   - a query that sees no key gets o = 0 and lse = -inf;
  *   - lse uses the natural logarithm;
