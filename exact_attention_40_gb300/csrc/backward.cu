@@ -52,20 +52,6 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk)
   return base + static_cast<uint32_t>(row * (D * 2)) + (static_cast<uint32_t>(chunk ^ (row & 7)) << 4);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Rows [row0, row0 + 64) of a [n_rows, D] bf16 matrix into a swizzled tile;
 // rows at or past n_rows read as zero (nothing is read for them).
 template <int D>

@@ -13,17 +13,27 @@
 // ("Optimizing LLM Inference ..." page, section Paged Attention and Dynamic
 // KV Cache Management); cache [num_blocks, Hkv, 16, d].
 //
-// One CTA per token (grid-stride; the d/2 frequencies are computed once per
-// CTA in fp64): every thread first loads its vectors of the token, then the
-// d/2 angles are formed and reduced
-// modulo 2 pi in fp64 (pos * inv_freq reaches 10^4 radians and more), then
-// cos/sin of the reduced angle in fp32 go to shared memory; each thread then
-// rotates 8 pairs at a time from two 16-byte vectors in fp32 and rounds once
-// to bf16.  q is rotated in place; k is read, rotated and written to the
-// cache only; v is copied to the cache.  A token whose sequence, position
-// or table entry lies outside the table or the cache writes nothing to the
-// cache and sets the bounds bit of the status word.
+// Persistent CTAs (as many as fit on the GPU at once), each walking every
+// G-th token.  Every thread copies its own 16-byte vectors of the CTA's
+// next tokens into shared memory with cp.async, two tokens ahead; thread
+// i < d/2 forms angle i of the current token reduced modulo 2 pi (pos *
+// theta_i reaches 10^4 radians and more) and puts its cos/sin, in fp32,
+// into shared memory (two buffers, so one barrier per token); each thread
+// then rotates 8 pairs at a time from its two staged vectors in fp32 and
+// rounds once to bf16.  The reduction needs no floating point per token:
+// u_i = base^(-2i/d) / (2 pi) is held as a 64-bit fixed-point fraction of
+// a turn (formed on the host, in fp64), and pos * u_i mod 2^64, an integer
+// multiply, is the angle in turns, its top 32 bits read as a signed
+// fraction in [-1/2, 1/2).  The error is u_i's fp64 rounding times pos
+// (below 1e-10 rad for positions under 2^20) plus the final fp32 rounding,
+// as with an fp64 product and reduction, and the fp64 pipe (slow on this
+// GPU) is not used at all.  q is rotated in place; k is read, rotated and
+// written to the cache only; v is copied to the cache.  A token whose
+// sequence, position or table entry lies outside the table or the cache
+// writes nothing to the cache and sets the bounds bit of the status word.
 #include <cuda_bf16.h>
+
+#include <cmath>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -47,18 +57,44 @@ __device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float* c, co
   hi = pack_bf16x8(yb);
 }
 
-// MAXI: work items per thread per token (q and k items are 8 pairs, v items
-// one 16-byte copy).  Each thread first issues the loads of all its items,
-// then the token's angles are formed, so the loads are in flight meanwhile.
-// (Two tokens per CTA step measured slower: fewer CTAs on a decode step and
-// more registers per thread.)
+constexpr int kRopeStages = 3;  // tokens per CTA whose copies are issued (two ahead of the one in use)
+
+// u_i = theta_i / (2 pi) per unit position, in units of 2^-64 turn, for
+// i < d/2; formed on the host once per call.
+struct RopeTurns {
+  unsigned long long u[kRopeMaxDim / 2];
+};
+
 template <int MAXI>
-__global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs a) {
-  __shared__ double inv_freq[kRopeMaxDim / 2];  // base^(-2i/d), the same for every token
-  __shared__ float cs[2][kRopeMaxDim / 2];        // cos, sin of this token's angles
+constexpr size_t rope_smem_bytes() {
+  return sizeof(float) * 2 * 2 * (kRopeMaxDim / 2) + sizeof(uint4) * kRopeStages * MAXI * 2 * kRopeThreads;
+}
+
+// Block-table entry of (seq, pos), or -1 when the pair lies outside the table.
+__device__ __forceinline__ int table_entry(const RopeArgs& a, int seq, int pos) {
+  if (seq < 0 || seq >= a.num_seqs || pos < 0 || pos / 16 >= a.max_blocks_per_seq) return -1;
+  return a.block_table[static_cast<long long>(seq) * a.max_blocks_per_seq + pos / 16];
+}
+
+// MAXI: work items per thread per token (q and k items are 8 pairs from
+// two 16-byte vectors, v items one 16-byte copy).  Each thread copies its
+// own vectors of the CTA's next tokens into its own shared-memory slots
+// with cp.async, kRopeStages - 1 tokens ahead of the one it rotates, so
+// the loads stay in flight without holding registers and need no barrier
+// (a thread reads back only what it copied).  The token metadata runs
+// ahead too: position and sequence two tokens ahead, the block-table entry
+// one token ahead, so no dependent load sits inside an iteration.  The one
+// barrier per token publishes the cos/sin of its angles (two buffers).
+template <int MAXI>
+__global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs a, const RopeTurns turns) {
+  extern __shared__ __align__(16) uint8_t rope_smem[];
+  float(*const cs)[2][kRopeMaxDim / 2] = reinterpret_cast<float(*)[2][kRopeMaxDim / 2]>(rope_smem);
+  uint4(*const stage)[MAXI][2][kRopeThreads] = reinterpret_cast<uint4(*)[MAXI][2][kRopeThreads]>(
+      rope_smem + sizeof(float) * 2 * 2 * (kRopeMaxDim / 2));
+  const int tid = threadIdx.x;
   const int d = a.d, half = d / 2, vec_half = half / 8, vec_d = d / 8;
-  for (int i = threadIdx.x; i < half; i += kRopeThreads) inv_freq[i] = exp2(-(2.0 * i / d) * a.log2_base);
-  __syncthreads();
+  // angle tid (if < half; half <= kRopeThreads)
+  const unsigned long long u_turn = tid < half ? turns.u[tid] : 0ull;
   uint4* q = static_cast<uint4*>(a.q);
   const uint4* k = static_cast<const uint4*>(a.k);
   const uint4* v = static_cast<const uint4*>(a.v);
@@ -66,68 +102,120 @@ __global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs
   uint4* vc = static_cast<uint4*>(a.v_cache);
   // q: Hq heads x vec_half items; k: Hkv heads x vec_half; v: Hkv x vec_d copies
   const int n_q = a.Hq * vec_half, n_k = a.Hkv * vec_half, n_all = n_q + n_k + a.Hkv * vec_d;
-  for (long long t = blockIdx.x; t < a.num_tokens; t += gridDim.x) {
-    uint4 lo[MAXI], hi[MAXI];
+  const long long G = gridDim.x, T = a.num_tokens;
+
+  // This thread's copies of token t into stage s; one commit group per call
+  // (empty past the last token), so the group count stays uniform.
+  auto issue = [&](long long t, int st) {
+    if (t < T) {
 #pragma unroll
-    for (int i = 0; i < MAXI; ++i) {
-      const int w = threadIdx.x + i * kRopeThreads;
-      if (w < n_q) {
-        const size_t row = (static_cast<size_t>(t) * a.Hq + w / vec_half) * vec_d + w % vec_half;
-        lo[i] = q[row];
-        hi[i] = q[row + vec_half];
-      } else if (w < n_q + n_k) {
-        const int item = w - n_q;
-        const size_t row = (static_cast<size_t>(t) * a.Hkv + item / vec_half) * vec_d + item % vec_half;
-        lo[i] = k[row];
-        hi[i] = k[row + vec_half];
-      } else if (w < n_all) {
-        const int item = w - n_q - n_k;
-        lo[i] = v[(static_cast<size_t>(t) * a.Hkv + item / vec_d) * vec_d + item % vec_d];
+      for (int i = 0; i < MAXI; ++i) {
+        const int w = tid + i * kRopeThreads;
+        const uint32_t lo = smem_u32(&stage[st][i][0][tid]), hi = smem_u32(&stage[st][i][1][tid]);
+        if (w < n_q) {
+          const size_t row = (static_cast<size_t>(t) * a.Hq + w / vec_half) * vec_d + w % vec_half;
+          cp_async16(lo, q + row, true);
+          cp_async16(hi, q + row + vec_half, true);
+        } else if (w < n_q + n_k) {
+          const int item = w - n_q;
+          const size_t row = (static_cast<size_t>(t) * a.Hkv + item / vec_half) * vec_d + item % vec_half;
+          cp_async16(lo, k + row, true);
+          cp_async16(hi, k + row + vec_half, true);
+        } else if (w < n_all) {
+          const int item = w - n_q - n_k;
+          cp_async16(lo, v + (static_cast<size_t>(t) * a.Hkv + item / vec_d) * vec_d + item % vec_d, true);
+        }
       }
     }
-    const int pos = a.positions[t];
-    const int seq = a.seq_ids[t];
-    long long slot = -1;  // block * 16 + offset
-    if (seq >= 0 && seq < a.num_seqs && pos >= 0 && pos / 16 < a.max_blocks_per_seq) {
-      const int blk = a.block_table[static_cast<long long>(seq) * a.max_blocks_per_seq + pos / 16];
-      if (blk >= 0 && blk < a.num_blocks) slot = static_cast<long long>(blk) * 16 + pos % 16;
-    }
-    if (slot < 0 && threadIdx.x == 0) atomicOr(a.status, 2u);  // EXATTN_DEVICE_BOUNDS_BIT
-    for (int i = threadIdx.x; i < half; i += kRopeThreads) {
-      const double ang = static_cast<double>(pos) * inv_freq[i];
-      const double r = ang - 6.283185307179586476925 * rint(ang * 0.159154943091895335769);
+    cp_async_commit();
+  };
+
+  long long t = blockIdx.x;
+#pragma unroll
+  for (int st = 0; st < kRopeStages - 1; ++st) issue(t + st * G, st);
+  int pos0 = t < T ? a.positions[t] : 0, seq0 = t < T ? a.seq_ids[t] : -1;
+  int pos1 = t + G < T ? a.positions[t + G] : 0, seq1 = t + G < T ? a.seq_ids[t + G] : -1;
+  int blk0 = table_entry(a, seq0, pos0);
+  for (int n = 0; t < T; ++n, t += G) {
+    issue(t + (kRopeStages - 1) * G, (n + kRopeStages - 1) % kRopeStages);
+    const int blk1 = table_entry(a, seq1, pos1);  // used in the next iteration
+    const long long t2 = t + 2 * G;
+    const int pos2 = t2 < T ? a.positions[t2] : 0, seq2 = t2 < T ? a.seq_ids[t2] : -1;
+
+    const long long slot = (blk0 >= 0 && blk0 < a.num_blocks) ? static_cast<long long>(blk0) * 16 + pos0 % 16 : -1;
+    if (slot < 0 && tid == 0) atomicOr(a.status, 2u);  // EXATTN_DEVICE_BOUNDS_BIT
+    float(*const csp)[kRopeMaxDim / 2] = cs[n & 1];
+    if (tid < half) {
+      const unsigned long long turn = static_cast<unsigned long long>(static_cast<long long>(pos0)) * u_turn;
+      const int top = static_cast<int>(static_cast<unsigned int>(turn >> 32));
+      const float r = static_cast<float>(top) * 1.46291807926715968e-9f;  // 2 pi / 2^32
       float sn, cn;
-      sincosf(static_cast<float>(r), &sn, &cn);
-      cs[0][i] = cn;
-      cs[1][i] = sn;
+      sincosf(r, &sn, &cn);
+      csp[0][tid] = cn;
+      csp[1][tid] = sn;
     }
+    cp_async_wait<kRopeStages - 1>();  // this thread's copies of token t have landed
+    // Publishes csp; the last reads of this buffer (two tokens ago)
+    // finished before the previous token's barrier.
     __syncthreads();
+
+    const int st = n % kRopeStages;
     const size_t cache_row =
         slot >= 0 ? (static_cast<size_t>(slot / 16) * a.Hkv * 16 + slot % 16) * vec_d : 0;
 #pragma unroll
     for (int i = 0; i < MAXI; ++i) {
-      const int w = threadIdx.x + i * kRopeThreads;
+      const int w = tid + i * kRopeThreads;
+      uint4 lo = stage[st][i][0][tid], hi = stage[st][i][1][tid];
       if (w < n_q) {
         const int j = w % vec_half;
-        rotate8(lo[i], hi[i], &cs[0][8 * j], &cs[1][8 * j]);
+        rotate8(lo, hi, &csp[0][8 * j], &csp[1][8 * j]);
         const size_t row = (static_cast<size_t>(t) * a.Hq + w / vec_half) * vec_d + j;
-        q[row] = lo[i];
-        q[row + vec_half] = hi[i];
+        q[row] = lo;
+        q[row + vec_half] = hi;
       } else if (w < n_q + n_k) {
         const int item = w - n_q, j = item % vec_half;
-        rotate8(lo[i], hi[i], &cs[0][8 * j], &cs[1][8 * j]);
+        rotate8(lo, hi, &csp[0][8 * j], &csp[1][8 * j]);
         if (slot >= 0) {
           const size_t dst = cache_row + static_cast<size_t>(item / vec_half) * 16 * vec_d + j;
-          kc[dst] = lo[i];
-          kc[dst + vec_half] = hi[i];
+          kc[dst] = lo;
+          kc[dst + vec_half] = hi;
         }
       } else if (w < n_all && slot >= 0) {
         const int item = w - n_q - n_k;
-        vc[cache_row + static_cast<size_t>(item / vec_d) * 16 * vec_d + item % vec_d] = lo[i];
+        vc[cache_row + static_cast<size_t>(item / vec_d) * 16 * vec_d + item % vec_d] = lo;
       }
     }
-    __syncthreads();  // cs is refilled for the next token
+    pos0 = pos1;
+    seq0 = seq1;
+    blk0 = blk1;
+    pos1 = pos2;
+    seq1 = seq2;
   }
+  cp_async_wait<0>();  // the groups still open are empty; none stays behind the CTA
+}
+
+template <int MAXI>
+cudaError_t launch_maxi(const RopeArgs& a, const RopeTurns& turns, int sms, cudaStream_t stream) {
+  constexpr size_t smem = rope_smem_bytes<MAXI>();
+  static int resident[64] = {};  // CTAs per SM, per device, set up on the device's first call
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    e = cudaFuncSetAttribute(rope_cache_kernel<MAXI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int r = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, rope_cache_kernel<MAXI>, kRopeThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (r < 1) return cudaErrorInvalidConfiguration;
+    resident[dev] = r;
+  }
+  const long long cap = static_cast<long long>(sms) * resident[dev];
+  const int grid = static_cast<int>(a.num_tokens < cap ? a.num_tokens : cap);
+  rope_cache_kernel<MAXI><<<grid, kRopeThreads, smem, stream>>>(a, turns);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -135,17 +223,20 @@ __global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs
 cudaError_t launch_rope_cache_write(const RopeArgs& a, cudaStream_t stream) {
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  const long long cap = static_cast<long long>(sms) * 8;
-  const int grid = static_cast<int>(a.num_tokens < cap ? a.num_tokens : cap);
+  if (a.d < 16 || a.d > kRopeMaxDim || a.d % 16 != 0) return cudaErrorInvalidValue;
+  // theta_i / (2 pi) * 2^64 = base^(-2i/d) * 2^64 / (2 pi), below 2^62, rounded to an integer
+  RopeTurns turns{};
+  for (int i = 0; i < a.d / 2; ++i)
+    turns.u[i] = static_cast<unsigned long long>(
+        std::nearbyint(std::exp2(-(2.0 * i / a.d) * a.log2_base) * (18446744073709551616.0 / 6.283185307179586476925)));
   const long long items = static_cast<long long>(a.Hq) * (a.d / 16) +
                           static_cast<long long>(a.Hkv) * (a.d / 16) + static_cast<long long>(a.Hkv) * (a.d / 8);
   const long long per_thread = (items + kRopeThreads - 1) / kRopeThreads;
-  if (per_thread <= 1) rope_cache_kernel<1><<<grid, kRopeThreads, 0, stream>>>(a);
-  else if (per_thread <= 2) rope_cache_kernel<2><<<grid, kRopeThreads, 0, stream>>>(a);
-  else if (per_thread <= 4) rope_cache_kernel<4><<<grid, kRopeThreads, 0, stream>>>(a);
-  else if (per_thread <= 8) rope_cache_kernel<8><<<grid, kRopeThreads, 0, stream>>>(a);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (per_thread <= 1) return launch_maxi<1>(a, turns, sms, stream);
+  if (per_thread <= 2) return launch_maxi<2>(a, turns, sms, stream);
+  if (per_thread <= 4) return launch_maxi<4>(a, turns, sms, stream);
+  if (per_thread <= 8) return launch_maxi<8>(a, turns, sms, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace exattn

@@ -242,7 +242,8 @@ int attn_graph_destroy(exattn_graph* graph);
  * of token t turn by theta_i = positions[t] * base^(-2i/d):
  *   y_i = x_i cos theta_i - x_(i+d/2) sin theta_i
  *   y_(i+d/2) = x_(i+d/2) cos theta_i + x_i sin theta_i
- * (angles reduced in fp64, rotation in fp32, one bf16 rounding).
+ * (angles reduced modulo 2 pi exactly in 64-bit fixed point from
+ * frequencies formed in fp64, rotation in fp32, one bf16 rounding).
  *   q        [num_tokens, Hq, d] bf16: rotated in place
  *   k, v     [num_tokens, Hkv, d] bf16: read only
  *   seq_ids, positions int32 [num_tokens]: sequence and 0-based position of

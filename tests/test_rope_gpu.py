@@ -101,6 +101,14 @@ def test_long_positions(env):
     run_case(env, inp, 2, 128, 10000.0)
 
 
+def test_positions_near_2_pow_20(env):
+    # angles up to ~1e6 radians, where the reduction modulo 2 pi is hardest;
+    # zeroed caches keep the 65,000-block cache copies cheap
+    inp = synth.rope_inputs_lens(55, [1 << 20, 3000], 4, 2, 1, 64)
+    run_case(env, inp, 1, 64, 500000.0, random_cache=False)
+    run_case(env, inp, 1, 64, 10000.0, random_cache=False)
+
+
 def test_decode_config(env):
     # the decode step of the paged-decode workload (64 sequences, 18101
     # blocks): all of q and every written slot against the oracle
