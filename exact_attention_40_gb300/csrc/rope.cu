@@ -16,11 +16,12 @@
 // Persistent CTAs (as many as fit on the GPU at once), each walking every
 // G-th token.  Every thread copies its own 16-byte vectors of the CTA's
 // next tokens into shared memory with cp.async, two tokens ahead; thread
-// i < d/2 forms angle i of the current token reduced modulo 2 pi (pos *
-// theta_i reaches 10^4 radians and more) and puts its cos/sin, in fp32,
-// into shared memory (two buffers, so one barrier per token); each thread
-// then rotates 8 pairs at a time from its two staged vectors in fp32 and
-// rounds once to bf16.  The reduction needs no floating point per token:
+// i < d/2 forms angle i of the next token reduced modulo 2 pi (pos *
+// theta_i reaches 10^4 radians and more) and puts its cos/sin (the
+// hardware fp32 approximation, within 4e-7 on the reduced angle) into
+// shared memory (two buffers, so one barrier per token); each thread then
+// rotates 8 pairs at a time from its two staged vectors in fp32 and rounds
+// once to bf16.  The reduction needs no floating point per token:
 // u_i = base^(-2i/d) / (2 pi) is held as a 64-bit fixed-point fraction of
 // a turn (formed on the host, in fp64), and pos * u_i mod 2^64, an integer
 // multiply, is the angle in turns, its top 32 bits read as a signed
@@ -77,14 +78,17 @@ __device__ __forceinline__ int table_entry(const RopeArgs& a, int seq, int pos) 
 }
 
 // MAXI: work items per thread per token (q and k items are 8 pairs from
-// two 16-byte vectors, v items one 16-byte copy).  Each thread copies its
-// own vectors of the CTA's next tokens into its own shared-memory slots
-// with cp.async, kRopeStages - 1 tokens ahead of the one it rotates, so
-// the loads stay in flight without holding registers and need no barrier
-// (a thread reads back only what it copied).  The token metadata runs
-// ahead too: position and sequence two tokens ahead, the block-table entry
-// one token ahead, so no dependent load sits inside an iteration.  The one
-// barrier per token publishes the cos/sin of its angles (two buffers).
+// two 16-byte vectors, v items one 16-byte copy); which items a thread owns
+// and where they sit within a token's rows is the same for every token and
+// worked out once.  Each thread copies its own vectors of the CTA's next
+// tokens into its own shared-memory slots with cp.async, kRopeStages - 1
+// tokens ahead of the one it rotates, so the loads stay in flight without
+// holding registers and need no barrier (a thread reads back only what it
+// copied).  The token metadata runs ahead too: position and sequence two
+// tokens ahead, the block-table entry one token ahead, so no dependent load
+// sits inside an iteration; and the cos/sin of the next token's angles are
+// formed right after the barrier that publishes the current token's, into
+// the other buffer, so that barrier does not wait for them.
 template <int MAXI>
 __global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs a, const RopeTurns turns) {
   extern __shared__ __align__(16) uint8_t rope_smem[];
@@ -100,34 +104,75 @@ __global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs
   const uint4* v = static_cast<const uint4*>(a.v);
   uint4* kc = static_cast<uint4*>(a.k_cache);
   uint4* vc = static_cast<uint4*>(a.v_cache);
-  // q: Hq heads x vec_half items; k: Hkv heads x vec_half; v: Hkv x vec_d copies
-  const int n_q = a.Hq * vec_half, n_k = a.Hkv * vec_half, n_all = n_q + n_k + a.Hkv * vec_d;
   const long long G = gridDim.x, T = a.num_tokens;
+  const size_t q_tok = static_cast<size_t>(a.Hq) * vec_d;    // 16-byte vectors per token of q
+  const size_t kv_tok = static_cast<size_t>(a.Hkv) * vec_d;  // ... of k or v
 
-  // This thread's copies of token t into stage s; one commit group per call
-  // (empty past the last token), so the group count stays uniform.
+  // Items: q heads x vec_half, then k heads x vec_half, then v heads x vec_d.
+  // kind 0 q, 1 k, 2 v, 3 none; off = vector within the token's rows; coff =
+  // vector within the token's cache rows (k, v); jv = first pair / 8 (q, k).
+  const int n_q = a.Hq * vec_half, n_k = a.Hkv * vec_half, n_all = n_q + n_k + a.Hkv * vec_d;
+  int kind[MAXI], off[MAXI], coff[MAXI], jv[MAXI];
+#pragma unroll
+  for (int i = 0; i < MAXI; ++i) {
+    const int w = tid + i * kRopeThreads;
+    kind[i] = 3;
+    off[i] = coff[i] = jv[i] = 0;
+    if (w < n_q) {
+      kind[i] = 0;
+      jv[i] = w % vec_half;
+      off[i] = (w / vec_half) * vec_d + jv[i];
+    } else if (w < n_q + n_k) {
+      const int item = w - n_q;
+      kind[i] = 1;
+      jv[i] = item % vec_half;
+      off[i] = (item / vec_half) * vec_d + jv[i];
+      coff[i] = (item / vec_half) * 16 * vec_d + jv[i];
+    } else if (w < n_all) {
+      const int item = w - n_q - n_k;
+      kind[i] = 2;
+      off[i] = item;
+      coff[i] = (item / vec_d) * 16 * vec_d + item % vec_d;
+    }
+  }
+
+  // This thread's copies of token t into stage st; one commit group per
+  // call (empty past the last token), so the group count stays uniform.
   auto issue = [&](long long t, int st) {
     if (t < T) {
+      const uint4* qs = q + static_cast<size_t>(t) * q_tok;
+      const uint4* ks = k + static_cast<size_t>(t) * kv_tok;
+      const uint4* vs = v + static_cast<size_t>(t) * kv_tok;
 #pragma unroll
       for (int i = 0; i < MAXI; ++i) {
-        const int w = tid + i * kRopeThreads;
         const uint32_t lo = smem_u32(&stage[st][i][0][tid]), hi = smem_u32(&stage[st][i][1][tid]);
-        if (w < n_q) {
-          const size_t row = (static_cast<size_t>(t) * a.Hq + w / vec_half) * vec_d + w % vec_half;
-          cp_async16(lo, q + row, true);
-          cp_async16(hi, q + row + vec_half, true);
-        } else if (w < n_q + n_k) {
-          const int item = w - n_q;
-          const size_t row = (static_cast<size_t>(t) * a.Hkv + item / vec_half) * vec_d + item % vec_half;
-          cp_async16(lo, k + row, true);
-          cp_async16(hi, k + row + vec_half, true);
-        } else if (w < n_all) {
-          const int item = w - n_q - n_k;
-          cp_async16(lo, v + (static_cast<size_t>(t) * a.Hkv + item / vec_d) * vec_d + item % vec_d, true);
+        if (kind[i] == 0) {
+          cp_async16(lo, qs + off[i], true);
+          cp_async16(hi, qs + off[i] + vec_half, true);
+        } else if (kind[i] == 1) {
+          cp_async16(lo, ks + off[i], true);
+          cp_async16(hi, ks + off[i] + vec_half, true);
+        } else if (kind[i] == 2) {
+          cp_async16(lo, vs + off[i], true);
         }
       }
     }
     cp_async_commit();
+  };
+  // cos/sin of angle tid of position pos into buffer buf.  pos * u mod 2^64
+  // is the angle in 2^-64 turns; its top 32 bits as a signed fraction of a
+  // turn times 2 pi give it in [-pi, pi), where the hardware sin/cos
+  // approximation is within 4e-7 absolute.
+  auto angles = [&](int pos, int buf) {
+    if (tid < half) {
+      const unsigned long long turn = static_cast<unsigned long long>(static_cast<long long>(pos)) * u_turn;
+      const int top = static_cast<int>(static_cast<unsigned int>(turn >> 32));
+      const float r = static_cast<float>(top) * 1.46291807926715968e-9f;  // 2 pi / 2^32
+      float sn, cn;
+      __sincosf(r, &sn, &cn);
+      cs[buf][0][tid] = cn;
+      cs[buf][1][tid] = sn;
+    }
   };
 
   long long t = blockIdx.x;
@@ -136,57 +181,43 @@ __global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs
   int pos0 = t < T ? a.positions[t] : 0, seq0 = t < T ? a.seq_ids[t] : -1;
   int pos1 = t + G < T ? a.positions[t + G] : 0, seq1 = t + G < T ? a.seq_ids[t + G] : -1;
   int blk0 = table_entry(a, seq0, pos0);
+  angles(pos0, 0);
   for (int n = 0; t < T; ++n, t += G) {
     issue(t + (kRopeStages - 1) * G, (n + kRopeStages - 1) % kRopeStages);
     const int blk1 = table_entry(a, seq1, pos1);  // used in the next iteration
     const long long t2 = t + 2 * G;
     const int pos2 = t2 < T ? a.positions[t2] : 0, seq2 = t2 < T ? a.seq_ids[t2] : -1;
-
     const long long slot = (blk0 >= 0 && blk0 < a.num_blocks) ? static_cast<long long>(blk0) * 16 + pos0 % 16 : -1;
     if (slot < 0 && tid == 0) atomicOr(a.status, 2u);  // EXATTN_DEVICE_BOUNDS_BIT
-    float(*const csp)[kRopeMaxDim / 2] = cs[n & 1];
-    if (tid < half) {
-      const unsigned long long turn = static_cast<unsigned long long>(static_cast<long long>(pos0)) * u_turn;
-      const int top = static_cast<int>(static_cast<unsigned int>(turn >> 32));
-      const float r = static_cast<float>(top) * 1.46291807926715968e-9f;  // 2 pi / 2^32
-      float sn, cn;
-      sincosf(r, &sn, &cn);
-      csp[0][tid] = cn;
-      csp[1][tid] = sn;
-    }
     cp_async_wait<kRopeStages - 1>();  // this thread's copies of token t have landed
-    // Publishes csp; the last reads of this buffer (two tokens ago)
-    // finished before the previous token's barrier.
+    // Publishes cs[n & 1]; every read of cs[(n + 1) & 1] (token t - G)
+    // happened before it, so the next token's angles may go there now.
     __syncthreads();
+    if (t + G < T) angles(pos1, (n + 1) & 1);
 
+    float(*const csp)[kRopeMaxDim / 2] = cs[n & 1];
     const int st = n % kRopeStages;
+    uint4* qd = q + static_cast<size_t>(t) * q_tok;
     const size_t cache_row =
         slot >= 0 ? (static_cast<size_t>(slot / 16) * a.Hkv * 16 + slot % 16) * vec_d : 0;
 #pragma unroll
     for (int i = 0; i < MAXI; ++i) {
-      const int w = tid + i * kRopeThreads;
       uint4 lo = stage[st][i][0][tid], hi = stage[st][i][1][tid];
-      if (w < n_q) {
-        const int j = w % vec_half;
-        rotate8(lo, hi, &csp[0][8 * j], &csp[1][8 * j]);
-        const size_t row = (static_cast<size_t>(t) * a.Hq + w / vec_half) * vec_d + j;
-        q[row] = lo;
-        q[row + vec_half] = hi;
-      } else if (w < n_q + n_k) {
-        const int item = w - n_q, j = item % vec_half;
-        rotate8(lo, hi, &csp[0][8 * j], &csp[1][8 * j]);
+      if (kind[i] == 0) {
+        rotate8(lo, hi, &csp[0][8 * jv[i]], &csp[1][8 * jv[i]]);
+        qd[off[i]] = lo;
+        qd[off[i] + vec_half] = hi;
+      } else if (kind[i] == 1) {
+        rotate8(lo, hi, &csp[0][8 * jv[i]], &csp[1][8 * jv[i]]);
         if (slot >= 0) {
-          const size_t dst = cache_row + static_cast<size_t>(item / vec_half) * 16 * vec_d + j;
-          kc[dst] = lo;
-          kc[dst + vec_half] = hi;
+          kc[cache_row + coff[i]] = lo;
+          kc[cache_row + coff[i] + vec_half] = hi;
         }
-      } else if (w < n_all && slot >= 0) {
-        const int item = w - n_q - n_k;
-        vc[cache_row + static_cast<size_t>(item / vec_d) * 16 * vec_d + item % vec_d] = lo;
+      } else if (kind[i] == 2 && slot >= 0) {
+        vc[cache_row + coff[i]] = lo;
       }
     }
     pos0 = pos1;
-    seq0 = seq1;
     blk0 = blk1;
     pos1 = pos2;
     seq1 = seq2;
