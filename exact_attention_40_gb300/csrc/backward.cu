@@ -202,14 +202,18 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
     }
     __syncthreads();
     const long long m0 = static_cast<long long>(qb_first + it) * kBwdRows;
-    // two halves of 32 queries: S^T = K Q^T, dP^T = V dO^T for this warp's
-    // 16 keys, then dV += P^T dO and dK += dS^T Q
+    // 16-query sub-blocks: S^T = K Q^T, dP^T = V dO^T for this warp's 16
+    // keys, then dV += P^T dO and dK += dS^T Q.  16 rather than 32 keeps
+    // S^T, dP^T and their bf16 fragments in 24 fewer registers next to the
+    // 128 dK/dV accumulators.
+    constexpr int kSub = 16;
+    constexpr int kNT = kSub / 8, kNP = kSub / 16;
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      const int c0 = 32 * half;
-      float st[4][4], dpt[4][4];
+    for (int sub = 0; sub < kBwdRows / kSub; ++sub) {
+      const int c0 = kSub * sub;
+      float st[kNT][4], dpt[kNT][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < kNT; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) st[i][e] = dpt[i][e] = 0.f;
 #pragma unroll
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
         lda<D>(s_k, warp * 16, kk, ak);
         lda<D>(s_v, warp * 16, kk, av);
 #pragma unroll
-        for (int np = 0; np < 2; ++np) {
+        for (int np = 0; np < kNP; ++np) {
           uint32_t bq[4], bd[4];
           ldb_nk<D>(s_q[buf], c0 + 16 * np, kk, bq);
           ldb_nk<D>(s_do[buf], c0 + 16 * np, kk, bd);
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
         }
       }
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = c0 + nt * 8 + 2 * t + (e & 1);
@@ -241,9 +245,9 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
           st[nt][e] = pt;
           dpt[nt][e] = pt * (dpt[nt][e] - s_ds[buf][col]);
         }
-      uint32_t pa[2][4], da[2][4];
+      uint32_t pa[kNP][4], da[kNP][4];
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
+      for (int kk = 0; kk < kNP; ++kk) {
         pa[kk][0] = pack_bf16x2(st[2 * kk][0], st[2 * kk][1]);
         pa[kk][1] = pack_bf16x2(st[2 * kk][2], st[2 * kk][3]);
         pa[kk][2] = pack_bf16x2(st[2 * kk + 1][0], st[2 * kk + 1][1]);
@@ -254,12 +258,12 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
         da[kk][3] = pack_bf16x2(dpt[2 * kk + 1][2], dpt[2 * kk + 1][3]);
       }
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
+      for (int kk = 0; kk < kNP; ++kk)
 #pragma unroll
         for (int np = 0; np < D / 16; ++np) {
           uint32_t bd[4], bq[4];
-          ldb_kn<D>(s_do[buf], 16 * np, 2 * half + kk, bd);
-          ldb_kn<D>(s_q[buf], 16 * np, 2 * half + kk, bq);
+          ldb_kn<D>(s_do[buf], 16 * np, c0 / 16 + kk, bd);
+          ldb_kn<D>(s_q[buf], 16 * np, c0 / 16 + kk, bq);
           mma_bf16_16816(dv[2 * np], pa[kk], bd[0], bd[1]);
           mma_bf16_16816(dv[2 * np + 1], pa[kk], bd[2], bd[3]);
           mma_bf16_16816(dk[2 * np], da[kk], bq[0], bq[1]);
