@@ -1,6 +1,7 @@
 // Internal launch interface between the C-ABI layer (api.cu) and the kernel
 // translation units.  Not part of the public ABI.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -11,15 +12,17 @@ namespace exattn {
 // Streaming multiprocessors of the current device (cached per device; 0 on
 // error).  Grids of the persistent and grid-stride kernels are sized by it.
 inline int device_sm_count() {
-  static int cached[64] = {};
+  // Launchers run outside the API lock: callers racing on a device's first
+  // query store the same value.
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 // Wait budget for every bounded pipeline wait inside the kernels.

@@ -228,22 +228,24 @@ __global__ void __launch_bounds__(kRopeThreads) rope_cache_kernel(const RopeArgs
 template <int MAXI>
 cudaError_t launch_maxi(const RopeArgs& a, const RopeTurns& turns, int sms, cudaStream_t stream) {
   constexpr size_t smem = rope_smem_bytes<MAXI>();
-  static int resident[64] = {};  // CTAs per SM, per device, set up on the device's first call
+  // CTAs per SM, per device, set up on the device's first call (callers
+  // racing on it set the same attribute and store the same value)
+  static std::atomic<int> resident[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (resident[dev] == 0) {
+  int r = resident[dev].load(std::memory_order_acquire);
+  if (r == 0) {
     e = cudaFuncSetAttribute(rope_cache_kernel<MAXI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    int r = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, rope_cache_kernel<MAXI>, kRopeThreads, smem);
     if (e != cudaSuccess) return e;
     if (r < 1) return cudaErrorInvalidConfiguration;
-    resident[dev] = r;
+    resident[dev].store(r, std::memory_order_release);
   }
-  const long long cap = static_cast<long long>(sms) * resident[dev];
+  const long long cap = static_cast<long long>(sms) * r;
   const int grid = static_cast<int>(a.num_tokens < cap ? a.num_tokens : cap);
   rope_cache_kernel<MAXI><<<grid, kRopeThreads, smem, stream>>>(a, turns);
   return cudaGetLastError();
