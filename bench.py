@@ -37,14 +37,31 @@ WORKLOAD = ("prefill llama3_8b_causal (B1 Hq32 Hkv8 Nq=Nk=2048 d128 causal) + "
 METRIC = "attn fwd TFLOP/s & % BF16 tensor peak; paged decode GB/s & % HBM peak"
 
 
+# Dense bf16 tensor rate of one SM: one M128 N128 K16 tcgen05.mma (524,288
+# FLOP) per 64 cycles.  A stand-alone loop issuing the prefill's MMAs back to
+# back sustains ~91% of it (about 2,240 cycles per 32 MMAs).
+BF16_FLOP_PER_CLK_PER_SM = 8192
+
+
+def bf16_peaks(peaks, sms, sm_mhz):
+    """The three bf16 denominators side by side; the roofline uses the first."""
+    theo = sms * BF16_FLOP_PER_CLK_PER_SM * sm_mhz * 1e6 / 1e12
+    return {"bf16_burst_measured": peaks["bf16"], "bf16_sustained_measured": peaks["bf16_sus"],
+            "bf16_theoretical": theo,
+            "theoretical_basis": "%d SMs x %d dense bf16 FLOP/clk/SM x %.0f MHz (SM clock during the "
+                                 "timed region)" % (sms, BF16_FLOP_PER_CLK_PER_SM, sm_mhz),
+            "used_for_roofline": "bf16_burst_measured (%s)" % peaks["src"]}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
         return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
-                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
-    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    sm_max_mhz=float(p.get("sm_max_mhz", 2070.0)), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max_mhz=2070.0, src="fallback")
 
 
 def load_traffic(kernel_file, key):
@@ -562,6 +579,9 @@ def run_gpu(args):
                      "traffic": load_traffic("rope.cu", "rope_cache_write_prefill_16k")}
     else:
         line_rope = None
+    sm_mhz = float(clocks["sm_mhz"]) if clocks and clocks.get("sm_mhz") else peaks["sm_max_mhz"]
+    bf16_side = bf16_peaks(peaks, torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count,
+                           sm_mhz)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -571,7 +591,10 @@ def run_gpu(args):
                    "l2": "flushed before every step (256 MiB write, outside the timed kernels)",
                    "wall_s_timed_region": t_wall},
         "prefill": {"tflops": achieved, "ms": pre_avg_ms,
-                    "frac_bf16_peak": achieved / peaks["bf16"], "flops": prefill_flops},
+                    "frac_bf16_peak": achieved / peaks["bf16"], "flops": prefill_flops,
+                    "peaks_tflops": bf16_side, "frac_of": {k: achieved / bf16_side[k] for k in
+                                                           ("bf16_burst_measured", "bf16_sustained_measured",
+                                                            "bf16_theoretical")}},
         "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_avg_ms,
                    "frac_hbm_peak": dec_gbs / world / peaks["hbm"],
                    "frac_8tbs": dec_gbs / world / 8000.0,
