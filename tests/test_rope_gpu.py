@@ -94,6 +94,14 @@ def test_head_sizes(env, d):
     run_case(env, inp, 1, d, 10000.0)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (128, 16)])
+def test_many_heads(env, Hq, Hkv):
+    # 704 and 1408 items per token at d = 128: four and eight per thread, the
+    # kernel variants with the deepest per-thread staging
+    inp = synth.rope_inputs_lens(56, [40, 300], 20, Hq, Hkv, 128)
+    run_case(env, inp, Hkv, 128, 500000.0)
+
+
 def test_long_positions(env):
     # positions up to 32767: the angles reach ~3e4 radians
     inp = synth.rope_inputs_lens(53, [32768, 20000], 8, 4, 2, 128)
