@@ -86,15 +86,17 @@ int device_state(int* dev, unsigned int** status) {
 
 // Descriptor of a bf16 tensor viewed as [planes, rows, d] (d innermost),
 // loaded/stored in boxes of box_rows rows x 64 columns with 128-byte
-// swizzle; rows past `rows` read as zero and are not written.  Caller holds
-// g_mu.
-int tensor_map(int dev, const void* ptr, int d, long long rows, long long planes,
-               const CUtensorMap** out, int box_rows = 128) {
+// swizzle; rows past `rows` read as zero and are not written.  The map is
+// copied to `out`, storage of the caller that outlives the launch: a later
+// lookup of the same call may clear the cache when it is full.  Caller
+// holds g_mu (and launches before releasing it).
+int tensor_map(int dev, const void* ptr, int d, long long rows, long long planes, CUtensorMap* out,
+               int box_rows = 128) {
   const MapKey key{reinterpret_cast<uintptr_t>(ptr), d, rows, planes, box_rows};
   auto& cache = g_maps[dev];
   auto it = cache.find(key);
   if (it != cache.end()) {
-    *out = &it->second;
+    *out = it->second;
     return EXATTN_OK;
   }
   if (cache.size() >= kMapCacheMax) cache.clear();
@@ -109,8 +111,8 @@ int tensor_map(int dev, const void* ptr, int d, long long rows, long long planes
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return EXATTN_ERR_CUDA;
-  auto ins = cache.emplace(key, m);
-  *out = &ins.first->second;
+  cache.emplace(key, m);
+  *out = m;
   return EXATTN_OK;
 }
 
@@ -177,19 +179,23 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
 
   exattn::PrefillArgs a;
   exattn::DeviceGuard g;
+  CUtensorMap map_q, map_k, map_v;  // copied into the launch's parameters
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
     int rc = device_state(&dev, &g.status);
     if (rc != EXATTN_OK) return rc;
     const long long pq = static_cast<long long>(B) * Hq, pk = static_cast<long long>(B) * Hkv;
-    if ((rc = tensor_map(dev, q, d, Nq, pq, &a.tm_q)) != EXATTN_OK) return rc;
+    if ((rc = tensor_map(dev, q, d, Nq, pq, &map_q)) != EXATTN_OK) return rc;
+    a.tm_q = &map_q;
     if (Nk > 0) {
-      if ((rc = tensor_map(dev, k, d, Nk, pk, &a.tm_k)) != EXATTN_OK) return rc;
-      if ((rc = tensor_map(dev, v, d, Nk, pk, &a.tm_v)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, k, d, Nk, pk, &map_k)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, v, d, Nk, pk, &map_v)) != EXATTN_OK) return rc;
+      a.tm_k = &map_k;
+      a.tm_v = &map_v;
     } else {
-      a.tm_k = a.tm_q;  // never dereferenced: no key tiles exist
-      a.tm_v = a.tm_q;
+      a.tm_k = &map_q;  // never dereferenced: no key tiles exist
+      a.tm_v = &map_q;
     }
     g.wait_ns = wait_budget_ns();
     a.out = out;
@@ -272,6 +278,7 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
 
   exattn::DecodeArgs a;
   exattn::DeviceGuard g;
+  CUtensorMap map_k, map_v;  // copied into the launch's parameters
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
@@ -279,8 +286,10 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
     if (rc != EXATTN_OK) return rc;
     // Each (block, kv head) span is 16 rows of the cache viewed as
     // [num_blocks * Hkv * 16, d]; one box = 16 rows x 64 columns.
-    if ((rc = tensor_map(dev, k_cache, d, cache_rows, 1, &a.tm_k, block_size)) != EXATTN_OK) return rc;
-    if ((rc = tensor_map(dev, v_cache, d, cache_rows, 1, &a.tm_v, block_size)) != EXATTN_OK) return rc;
+    if ((rc = tensor_map(dev, k_cache, d, cache_rows, 1, &map_k, block_size)) != EXATTN_OK) return rc;
+    if ((rc = tensor_map(dev, v_cache, d, cache_rows, 1, &map_v, block_size)) != EXATTN_OK) return rc;
+    a.tm_k = &map_k;
+    a.tm_v = &map_v;
     g.wait_ns = wait_budget_ns();
     const int splits = decode_max_splits(max_blocks_per_seq, block_size);
     a.q = q;
