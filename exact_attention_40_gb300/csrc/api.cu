@@ -501,7 +501,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0) return EXATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !good_scale(scale)) return EXATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return EXATTN_ERR_UNSUPPORTED;
-  if (Nq > (1 << 30) || Nk > (1 << 30) || static_cast<long long>(B) * Hq > 65535 ||
+  // 64-row blocks of either length index the second grid dimension (<= 65535)
+  if (Nq > 65535 * 64 || Nk > 65535 * 64 || static_cast<long long>(B) * Hq > 65535 ||
       static_cast<long long>(B) * Hkv > 65535)
     return EXATTN_ERR_UNSUPPORTED;
   if (B == 0 || (Nq == 0 && Nk == 0)) return EXATTN_OK;

@@ -196,7 +196,8 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  *   workspace: attn_bwd_workspace_bytes(...) bytes, 16-byte aligned (its
  *   contents need not be initialised and are clobbered)
  * scale, causal (same bottom-right mask), d and the head counts as attn_fwd;
- * B*Hq, B*Hkv <= 65535.  All tensor pointers 16-byte aligned (lse 4); no
+ * B*Hq, B*Hkv <= 65535 and Nq, Nk <= 65535 * 64 (EXATTN_ERR_UNSUPPORTED
+ * beyond).  All tensor pointers 16-byte aligned (lse 4); no
  * output may overlap an input.  B == 0 or Nq == Nk == 0 launches nothing.
  * Up to four kernel launches on `stream` (D, dk/dv, their sum over query
  * heads when Hq > Hkv, dq); asynchronous, deterministic (no atomics).

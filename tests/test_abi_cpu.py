@@ -220,4 +220,7 @@ def test_bwd_rejections_and_workspace(lib):
     assert bwd(lib, ws=None) == 4
     assert bwd(lib, ws_bytes=8) == 4
     assert bwd(lib, B=70000) == 2
+    # 64-row blocks of a length index the second grid dimension
+    assert bwd(lib, Nk=65535 * 64 + 1) == 2
+    assert bwd(lib, Nq=65535 * 64 + 1) == 2
     assert bwd(lib, B=0, q=None) == 0
