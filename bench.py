@@ -9,8 +9,12 @@ step; the flush is outside the timed kernels.  Each kernel group is timed
 with CUDA events on the launching stream.
 
 Prints one JSON line (rank 0).  `value` is prefill TFLOP/s (causal FLOPs
-4*B*Hq*Nq*Nk*d/2 over the summed prefill kernel time, summed over ranks);
-decode HBM GB/s is reported under "decode".
+4*B*Hq*Nq*Nk*d/2 over the summed prefill kernel time of the K timed steps,
+summed over ranks); decode HBM GB/s is reported under "decode"; the median
+and range of the per-step times sit beside both.  The other prefill
+configurations (tiny, batched B8 x H32 x N4096 in four variants, 32K-token
+causal) are timed apart from the step under "prefill_configs", as are the
+backward, the RMS norm, the RoPE cache write and the decode graph.
 
 --impl reference times the fp64 CPU oracle on this host's cores instead,
 each step on a bounded sample of the same prefill workload.
@@ -36,6 +40,8 @@ WORKLOAD = ("prefill llama3_8b_causal (B1 Hq32 Hkv8 Nq=Nk=2048 d128 causal) + "
             "paged decode (64 seqs, ctx U[512,8192], Hq32 Hkv8 d128, 16-token blocks)")
 METRIC = "attn fwd TFLOP/s & % BF16 tensor peak; paged decode GB/s & % HBM peak"
 
+
+BWD_KERNELS = "dsum + dK/dV + dQ (mma.sync)"
 
 # Dense bf16 tensor rate of one SM: one M128 N128 K16 tcgen05.mma (524,288
 # FLOP) per 64 cycles.  A stand-alone loop issuing the prefill's MMAs back to
@@ -159,6 +165,26 @@ def max_over_ranks(x, world, device):
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def spread(ms):
+    """Mean, median, min and max of per-call CUDA-event times (ms)."""
+    return {"ms_mean": statistics.fmean(ms), "ms_median": statistics.median(ms), "ms_min": min(ms),
+            "ms_max": max(ms), "calls": len(ms)}
+
+
+def timed_calls(torch, fn, calls, flush, stream):
+    """CUDA-event time (ms) of each of `calls` calls of fn on `stream`, L2
+    flushed (a write larger than L2) before each, outside the events."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(calls)]
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
 def prefill_row_flops(rows, Nq, Nk, d, causal):
@@ -308,6 +334,7 @@ def run_gpu(args):
     pre_avg_ms = pre_total / args.steps
     dec_avg_ms = dec_total / args.steps
     achieved = prefill_flops / (pre_avg_ms * 1e-3) / 1e12
+    pre_spread, dec_spread = spread(pre_ms), spread(dec_ms)
 
     # ---- the decode step replayed from a captured CUDA graph (same kernels,
     # same buffers), L2 flushed before every replay, apart from the step
@@ -383,22 +410,70 @@ def run_gpu(args):
         for _ in range(3):
             exattn.attn_bwd(q, k, v, out, dod, lse, causal=True, dq=bdq, dk=bdk, dv=bdv, workspace=bws)
         torch.cuda.synchronize()
-        bevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.bwd_calls)]
-        for e0, e1 in bevs:
-            flush.fill_(1)
-            e0.record(stream)
-            exattn.attn_bwd(q, k, v, out, dod, lse, causal=True, dq=bdq, dk=bdk, dv=bdv, workspace=bws)
-            e1.record(stream)
-        torch.cuda.synchronize()
+        b_list = timed_calls(torch, lambda: exattn.attn_bwd(q, k, v, out, dod, lse, causal=True, dq=bdq, dk=bdk,
+                                                            dv=bdv, workspace=bws),
+                             args.bwd_calls, flush, stream)
         if exattn.attn_get_device_status() != 0:
             raise RuntimeError("device status word set by attn_bwd")
-        b_ms = sum(e0.elapsed_time(e1) for e0, e1 in bevs) / args.bwd_calls
+        b_st = spread(b_list)
+        b_ms = b_st["ms_mean"]
         b_flops = 2.5 * prefill_flops
         bwd = {"workload": "llama3_8b_causal", "tflops": b_flops / (b_ms * 1e-3) / 1e12, "ms": b_ms,
+               "tflops_median": b_flops / (b_st["ms_median"] * 1e-3) / 1e12, "per_call": b_st,
                "flops": b_flops, "frac_bf16_peak": b_flops / (b_ms * 1e-3) / 1e12 / peaks["bf16"],
-               "calls": args.bwd_calls, "kernels": "dsum + dK/dV + dQ (mma.sync)"}
+               "calls": args.bwd_calls, "kernels": BWD_KERNELS}
         del dod, bdq, bdk, bdv, bws
+
+    # ---- every prefill configuration, timed apart from the step: the tiny
+    # case, the batched B8 x H32 x N4096 shape (non-causal and causal, and the
+    # variants with Q scaled by 8) and the 32K-token causal prefill.  Each
+    # call is timed with CUDA events, L2 flushed before it; the inputs of the
+    # batched and long shapes are larger than L2 anyway.
+    configs = None
+    if args.config_calls > 0:
+        configs = {}
+        groups = (("tiny", ("tiny",)), ("batched", ("batched_noncausal", "batched_causal",
+                                                   "batched_stab_noncausal", "batched_stab_causal")),
+                  ("long_causal", ("long_causal",)))
+        for gname, names in groups:
+            cfg0 = synth.PREFILL[names[0]]
+            gq, gk, gv = (to_dev(a) for a in synth.prefill_inputs(cfg0))
+            gout = torch.empty_like(gq)
+            glse = torch.empty((cfg0.B, cfg0.Hq, cfg0.N), device=dev, dtype=torch.float32)
+            gq8 = gq * 8 if any(synth.PREFILL[n].q_mult != 1.0 for n in names) else None  # exact in bf16
+            csampler = ClockSampler(local) if rank == 0 else None
+            if csampler:
+                csampler.start()
+                time.sleep(0.3)
+            for name in names:
+                cfg = synth.PREFILL[name]
+                qin = gq8 if cfg.q_mult != 1.0 else gq
+
+                def call(qin=qin, cfg=cfg):
+                    exattn.attn_fwd(qin, gk, gv, causal=cfg.causal, out=gout, lse=glse)
+
+                for _ in range(3):
+                    call()
+                ms = timed_calls(torch, call, args.config_calls if cfg.N > 128 else 10 * args.config_calls,
+                                 flush, stream)
+                st = spread(ms)
+                fl = cfg.flops()
+                configs[name] = dict(
+                    shape="B%d Hq%d Hkv%d Nq=Nk=%d d%d %s%s" % (cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.d,
+                                                             "causal" if cfg.causal else "non-causal",
+                                                             ", Q x8" if cfg.q_mult != 1.0 else ""),
+                    flops=fl, tflops=fl / (st["ms_mean"] * 1e-3) / 1e12,
+                    tflops_median=fl / (st["ms_median"] * 1e-3) / 1e12,
+                    tflops_min_max=[fl / (st["ms_max"] * 1e-3) / 1e12, fl / (st["ms_min"] * 1e-3) / 1e12],
+                    frac_bf16_burst=fl / (st["ms_mean"] * 1e-3) / 1e12 / peaks["bf16"],
+                    frac_bf16_sustained=fl / (st["ms_mean"] * 1e-3) / 1e12 / peaks["bf16_sus"], **st)
+            torch.cuda.synchronize()
+            cl_ = csampler.stop() if csampler else None
+            for name in names:
+                configs[name]["clocks"] = cl_
+            if exattn.attn_get_device_status() != 0:
+                raise RuntimeError("device status word set by the %s configurations" % gname)
+            del gq, gk, gv, gout, glse, gq8
 
     # ---- end to end through the public API with pinned host buffers.  Every
     # step copies its q, k, v in from pinned host memory and reads its out
@@ -590,12 +665,14 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed before every step (256 MiB write, outside the timed kernels)",
                    "wall_s_timed_region": t_wall},
-        "prefill": {"tflops": achieved, "ms": pre_avg_ms,
+        "prefill": {"tflops": achieved, "ms": pre_avg_ms, "per_step": pre_spread,
+                    "tflops_median": prefill_flops / (pre_spread["ms_median"] * 1e-3) / 1e12,
                     "frac_bf16_peak": achieved / peaks["bf16"], "flops": prefill_flops,
                     "peaks_tflops": bf16_side, "frac_of": {k: achieved / bf16_side[k] for k in
                                                            ("bf16_burst_measured", "bf16_sustained_measured",
                                                             "bf16_theoretical")}},
-        "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_avg_ms,
+        "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_avg_ms, "per_step": dec_spread,
+                   "gbs_median": decode_bytes / (dec_spread["ms_median"] * 1e-3) / 1e9,
                    "frac_hbm_peak": dec_gbs / world / peaks["hbm"],
                    "frac_8tbs": dec_gbs / world / 8000.0,
                    "kv_bytes": decode_bytes, "all_bytes": decode_bytes_all},
@@ -615,6 +692,7 @@ def run_gpu(args):
         "rope_cache_write": rope,
         "decode_graph": dgraph,
         "attn_bwd": bwd,
+        "prefill_configs": configs,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
@@ -638,6 +716,8 @@ def main():
                     help="attn_rope_cache_write calls for the decode step (0 skips it)")
     ap.add_argument("--norm-calls", type=int, default=200,
                     help="add_rms_norm calls per shape (0 skips that measurement)")
+    ap.add_argument("--config-calls", type=int, default=10,
+                    help="calls per prefill configuration timed apart (tiny, batched x4, 32K); 0 skips")
     ap.add_argument("--ref-rows-total", type=int, default=60000,
                     help="reference arm: query rows spread over all steps")
     args = ap.parse_args()

@@ -197,23 +197,22 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
       a.tm_k = &map_q;  // never dereferenced: no key tiles exist
       a.tm_v = &map_q;
     }
-    g.wait_ns = wait_budget_ns();
-    a.out = out;
-    a.lse = lse;
-    a.B = B;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.Nq = Nq;
-    a.Nk = Nk;
-    a.d = d;
-    a.causal = causal ? 1 : 0;
-    a.scale = scale;
-    // Launch while holding the lock: the descriptors are copied into the
-    // kernel's parameters at launch, so a concurrent cache eviction cannot
-    // invalidate them afterwards.
-    if (exattn::launch_prefill(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return EXATTN_ERR_CUDA;
   }
+  // The lock covers only the cache lookups: the maps are this call's own
+  // copies, so another thread's cache eviction cannot touch them.
+  g.wait_ns = wait_budget_ns();
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  if (exattn::launch_prefill(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXATTN_ERR_CUDA;
   return EXATTN_OK;
 }
 
@@ -288,9 +287,12 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
     // [num_blocks * Hkv * 16, d]; one box = 16 rows x 64 columns.
     if ((rc = tensor_map(dev, k_cache, d, cache_rows, 1, &map_k, block_size)) != EXATTN_OK) return rc;
     if ((rc = tensor_map(dev, v_cache, d, cache_rows, 1, &map_v, block_size)) != EXATTN_OK) return rc;
-    a.tm_k = &map_k;
-    a.tm_v = &map_v;
-    g.wait_ns = wait_budget_ns();
+  }
+  // The maps are this call's own copies: the launch needs no lock.
+  a.tm_k = &map_k;
+  a.tm_v = &map_v;
+  g.wait_ns = wait_budget_ns();
+  {
     const int splits = decode_max_splits(max_blocks_per_seq, block_size);
     a.q = q;
     a.k_cache = k_cache;
@@ -310,11 +312,9 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.max_splits = splits;
     a.scale = scale;
-    // launched under the lock: the descriptors are copied into the kernel
-    // parameters at launch
-    if (exattn::launch_decode(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return EXATTN_ERR_CUDA;
   }
+  if (exattn::launch_decode(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXATTN_ERR_CUDA;
   return EXATTN_OK;
 }
 
@@ -389,8 +389,14 @@ int attn_decode_paged_static(const void* q, const void* k_cache, const void* v_c
                              const int32_t* block_table, const int32_t* ctx_lens, void* out,
                              float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
                              int num_blocks, int max_blocks_per_seq, float scale, void* stream) {
-  const size_t need = attn_decode_workspace_bytes(num_seqs, Hq, d, max_blocks_per_seq, block_size);
-  if (need > EXATTN_STATIC_SCRATCH_BYTES) return EXATTN_ERR_WORKSPACE;
+  // Every argument is checked on the host before any CUDA call, against a
+  // stand-in for the static array (aligned, never dereferenced) of its
+  // size: a request that needs more scratch fails with EXATTN_ERR_WORKSPACE.
+  alignas(16) static unsigned char stand_in[16];
+  const int vrc = decode_validate(q, k_cache, v_cache, block_table, ctx_lens, out, lse, num_seqs, Hq, Hkv,
+                                  d, block_size, num_blocks, max_blocks_per_seq, scale, stand_in,
+                                  EXATTN_STATIC_SCRATCH_BYTES);
+  if (vrc != EXATTN_OK || num_seqs == 0) return vrc;
   void* scratch = nullptr;
   {
     // Once per device, with that device current: the host-side name of the
@@ -406,8 +412,7 @@ int attn_decode_paged_static(const void* q, const void* k_cache, const void* v_c
     }
     scratch = g_static_scratch_ptr[dev];
   }
-  // Same validation and kernels as the workspace entry point (need == 0
-  // means the arguments are invalid, and it reports which).
+  // Same kernels as the workspace entry point.
   return attn_decode_paged(q, k_cache, v_cache, block_table, ctx_lens, out, lse, num_seqs, Hq, Hkv,
                            d, block_size, num_blocks, max_blocks_per_seq, scale, scratch,
                            EXATTN_STATIC_SCRATCH_BYTES, stream);
@@ -505,6 +510,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   if (Nq > 65535 * 64 || Nk > 65535 * 64 || static_cast<long long>(B) * Hq > 65535 ||
       static_cast<long long>(B) * Hkv > 65535)
     return EXATTN_ERR_UNSUPPORTED;
+  // the one-dimensional grids of the D and reduce kernels stay below 2^31
+  if ((static_cast<long long>(B) * Hq * Nq + 7) / 8 > 0x7FFFFFFFll ||
+      (static_cast<long long>(B) * Hkv * Nk * d / 4 + 255) / 256 > 0x7FFFFFFFll)
+    return EXATTN_ERR_UNSUPPORTED;
   if (B == 0 || (Nq == 0 && Nk == 0)) return EXATTN_OK;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr ||
       lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
@@ -541,13 +550,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   return EXATTN_OK;
 }
 
-int attn_get_device_status(void* stream, unsigned int* status_out) {
+int attn_get_device_status(void* stream, int* status_out) {
   if (status_out == nullptr) return EXATTN_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;
   unsigned int v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return EXATTN_ERR_CUDA;
   if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return EXATTN_ERR_CUDA;
-  *status_out = v;
+  *status_out = static_cast<int>(v & 0x7FFFFFFFu);
   return EXATTN_OK;
 }
 

@@ -442,9 +442,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
         static_cast<const __nv_bfloat16*>(a.out), p.dout, a.dsum, rows);
   }
   const int smem = 6 * kBwdRows * D * 2;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<int> smem_dkdv[64] = {}, smem_dq[64] = {};
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(bwd_dkdv_kernel<D>), smem, smem_dkdv);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = smem_limit_once(reinterpret_cast<const void*>(bwd_dq_kernel<D>), smem, smem_dq);
   if (e != cudaSuccess) return e;
   const int G = a.Hq / a.Hkv;
   p.part = G > 1 ? a.part : nullptr;

@@ -382,9 +382,9 @@ cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t str
   sp.max_splits = a.max_splits;
   sp.scale_log2 = a.scale * kLog2e;
   const size_t smem = split_smem_bytes<D>();
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static std::atomic<int> smem_set[64] = {};
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(decode_split_kernel<D>),
+                                  static_cast<int>(smem), smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_splits, a.Hkv * sp.n_chunks, a.num_seqs);
   decode_split_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_k, *a.tm_v, sp);

@@ -25,6 +25,20 @@ inline int device_sm_count() {
   return n;
 }
 
+// Raises `func`'s dynamic shared-memory limit to `bytes` once per device:
+// `done` is the calling launcher's own per-device record of the value set
+// (callers racing on a device's first launch set the same attribute).
+inline cudaError_t smem_limit_once(const void* func, int bytes, std::atomic<int> (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire) == bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(bytes, std::memory_order_release);
+  return e;
+}
+
 // Wait budget for every bounded pipeline wait inside the kernels.
 struct DeviceGuard {
   unsigned int* status;        // device status word (OR of EXATTN_DEVICE_*_BIT)

@@ -611,8 +611,9 @@ cudaError_t launch_d(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t st
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const size_t smem = smem_bytes_for<D>();
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  static std::atomic<int> smem_set[64] = {};
+  const cudaError_t e =
+      smem_limit_once(reinterpret_cast<const void*>(prefill_kernel<D>), static_cast<int>(smem), smem_set);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (each holds all 512 TMEM columns)
   const int grid = static_cast<int>(min(n_items, static_cast<long long>(sms)));

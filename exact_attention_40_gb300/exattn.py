@@ -41,7 +41,7 @@ lib.attn_decode_paged.restype = _I
 lib.attn_decode_paged_static.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                          _F, _P]
 lib.attn_decode_paged_static.restype = _I
-lib.attn_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
+lib.attn_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int)]
 lib.attn_get_device_status.restype = _I
 lib.attn_status_string.argtypes = [_I]
 lib.attn_status_string.restype = ctypes.c_char_p
@@ -353,7 +353,7 @@ def attn_bwd(q, k, v, out, dout, lse, causal: bool = False, scale: float | None 
 
 def attn_get_device_status(stream=None) -> int:
     """Synchronise the stream, then read and clear the device status word."""
-    v = ctypes.c_uint(0)
+    v = ctypes.c_int(0)
     rc = lib.attn_get_device_status(_stream_handle(stream), ctypes.byref(v))
     if rc != EXATTN_OK:
         raise ExattnError("attn_get_device_status", rc)

@@ -270,10 +270,12 @@ int attn_rope_cache_write(void* q, const void* k, const void* v, const int32_t* 
 
 /*
  * Synchronises `stream`, then reads and clears the status word of the
- * current device: 0, or an OR of EXATTN_DEVICE_*_BIT.  Returns EXATTN_OK
+ * current device and stores it in *status_out: 0, or an OR of
+ * EXATTN_DEVICE_*_BIT (the bits are small, so the value is never negative).
+ * status_out must not be NULL (EXATTN_ERR_INVALID_ARG).  Returns EXATTN_OK
  * or EXATTN_ERR_CUDA.
  */
-int attn_get_device_status(void* stream, unsigned int* status_out);
+int attn_get_device_status(void* stream, int* status_out);
 
 /* Human-readable name of an exattn_status value (static string). */
 const char* attn_status_string(int status);

@@ -111,6 +111,39 @@ def test_decode_rejections(lib):
     assert dec(lib, S=70000) == 2
 
 
+def dec_static(lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, cl=FAKE, out=FAKE, lse=None, S=2, Hq=8, Hkv=2,
+             d=128, bs=16, nb=10, mb=4, scale=0.1)
+    a.update(kw)
+    return lib.lib.attn_decode_paged_static(a["q"], a["kc"], a["vc"], a["bt"], a["cl"], a["out"],
+                                            a["lse"], a["S"], a["Hq"], a["Hkv"], a["d"], a["bs"],
+                                            a["nb"], a["mb"], a["scale"], None)
+
+
+def test_decode_static_rejections_before_any_cuda_call(lib):
+    # the same host checks as attn_decode_paged, run before the scratch
+    # array's address is looked up (no GPU here: a CUDA call would fail with
+    # EXATTN_ERR_CUDA instead)
+    assert dec_static(lib, bs=32) == 2
+    assert dec_static(lib, d=80) == 2
+    assert dec_static(lib, Hq=6, Hkv=4) == 1
+    assert dec_static(lib, mb=0) == 1
+    assert dec_static(lib, nb=0) == 1
+    assert dec_static(lib, scale=0.0) == 1
+    assert dec_static(lib, kc=None) == 1
+    assert dec_static(lib, bt=FAKE + 2) == 3
+    assert dec_static(lib, q=FAKE + 4) == 3
+    assert dec_static(lib, S=70000) == 2
+    assert dec_static(lib, S=0, q=None) == 0
+    # more scratch than the static array holds
+    assert lib.attn_decode_workspace_bytes(4096, 64, 128, 512) > 32 * 2 ** 20
+    assert dec_static(lib, S=4096, Hq=64, Hkv=8, mb=512) == 4
+
+
+def test_device_status_needs_an_output(lib):
+    assert lib.lib.attn_get_device_status(None, None) == 1
+
+
 def test_debug_wait_budget_validated(lib):
     assert lib.lib.attn_debug_expire_wait(0, None) == 1
     assert lib.lib.attn_debug_expire_wait(10 ** 11, None) == 1
@@ -223,4 +256,7 @@ def test_bwd_rejections_and_workspace(lib):
     # 64-row blocks of a length index the second grid dimension
     assert bwd(lib, Nk=65535 * 64 + 1) == 2
     assert bwd(lib, Nq=65535 * 64 + 1) == 2
+    # one-dimensional grids of 2^31 blocks or more
+    assert bwd(lib, B=1, Hq=65535, Hkv=65535, Nq=65535 * 64, Nk=8) == 2
+    assert bwd(lib, B=1, Hq=65535, Hkv=65535, Nq=8, Nk=65535 * 64) == 2
     assert bwd(lib, B=0, q=None) == 0

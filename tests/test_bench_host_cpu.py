@@ -55,3 +55,10 @@ def test_bf16_peaks_side_by_side():
     # 152 SMs x 8192 FLOP/clk x 2.07 GHz
     assert side["bf16_theoretical"] == pytest.approx(2577.53088, rel=1e-12)
     assert side["used_for_roofline"].startswith("bf16_burst_measured")
+
+
+def test_spread_of_per_step_times():
+    st = bench.spread([3.0, 1.0, 2.0, 10.0])
+    assert st["ms_mean"] == 4.0
+    assert st["ms_median"] == 2.5
+    assert (st["ms_min"], st["ms_max"], st["calls"]) == (1.0, 10.0, 4)

@@ -93,7 +93,7 @@ def _sampled(env, name, per_head):
 @pytest.mark.parametrize("name", ["batched_noncausal", "batched_causal",
                                   "batched_stab_noncausal", "batched_stab_causal"])
 def test_batched_sampled(env, name):
-    _sampled(env, name, 16)
+    _sampled(env, name, 256)
 
 
 def test_long_context_sampled(env):
