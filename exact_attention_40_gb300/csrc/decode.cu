@@ -17,7 +17,8 @@
 //   heads of the GQA group are the 16 rows, padded with zeros), keeping an
 //   online softmax (running max m, sum l) on the accumulator fragments.  At
 //   the end the warps' states merge in shared memory and the split writes
-//   its normalised partial output O_s and lse_s (natural log) to the
+//   its partial output O_s (divided by the sum of the bf16 weights P V used)
+//   and lse_s (natural log, from the unrounded exponentials) to the
 //   workspace.
 // decode_combine_kernel: one CTA per (sequence, query head):
 //   L = log sum_s exp(lse_s), o = sum_s exp(lse_s - L) O_s, lse = L.
@@ -50,6 +51,7 @@ struct alignas(1024) DecodeSmem {
   uint8_t ring[kWarps][kStages][kStageBytes];
   float wm[kWarps][kRows];  // per-warp running max (log2 units)
   float wl[kWarps][kRows];  // per-warp running sum
+  float wlr[kWarps][kRows]; // per-warp running sum of the bf16-rounded weights
   uint64_t full[kWarps][kStages];
 };
 
@@ -177,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   float m[2] = {-INFINITY, -INFINITY};  // rows g, g + 8 (log2 units)
-  float l[2] = {0.f, 0.f};              // this thread's partial sums
+  float l[2] = {0.f, 0.f};              // this thread's partial sums of the exponentials
+  float lr[2] = {0.f, 0.f};             // ... and of their bf16 roundings (what P V uses)
   float acc[kNTiles][4];
 #pragma unroll
   for (int n = 0; n < kNTiles; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
@@ -240,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         l[r] = l[r] * alpha[r] + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
         pa[r] = pack_bf16x2(pr[0], pr[1]);      // a0 (row g) / a1 (row g + 8): tokens 2t, 2t+1
         pa[2 + r] = pack_bf16x2(pr[2], pr[3]);  // a2 / a3: tokens 8 + 2t, 8 + 2t + 1
+        lr[r] = lr[r] * alpha[r] + ((__uint_as_float(pa[r] << 16) + __uint_as_float(pa[r] & 0xFFFF0000u)) +
+                                    (__uint_as_float(pa[2 + r] << 16) + __uint_as_float(pa[2 + r] & 0xFFFF0000u)));
       }
 #pragma unroll
       for (int n = 0; n < kNTiles; ++n) {
@@ -274,17 +279,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (issued < my_n) issue(issued++);
   }
 
-  // ---- per-warp totals of l (the four lanes of a row group)
+  // ---- per-warp totals of l and l_r (the four lanes of a row group)
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
     l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+    lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 1);
+    lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
   }
   if (t == 0) {
     sm.wm[warp][g] = m[0];
     sm.wm[warp][g + 8] = m[1];
     sm.wl[warp][g] = l[0];
     sm.wl[warp][g + 8] = l[1];
+    sm.wlr[warp][g] = lr[0];
+    sm.wlr[warp][g + 8] = lr[1];
   }
   __syncthreads();  // every warp finished streaming: the rings are free
   float* wacc = reinterpret_cast<float*>(&sm.ring[0][0][0]);  // [warp][row][D]
@@ -303,17 +312,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][r]);
-    float L = 0.f, o = 0.f;
+    float L = 0.f, Lr = 0.f, o = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float wt = (sm.wm[w][r] == -INFINITY) ? 0.f : ex2_approx(sm.wm[w][r] - M);
         L += wt * sm.wl[w][r];
+        Lr += wt * sm.wlr[w][r];
         o += wt * wacc[(w * kRows + r) * D + col];
       }
     }
     const size_t slot = (static_cast<size_t>(seq) * p.Hq + hq0 + r) * p.max_splits + split;
-    p.ws_o[slot * D + col] = (L > 0.f) ? o / L : 0.f;
+    // the split's output divides by the sum of the weights P V used; its
+    // log-sum-exp keeps the sum of the unrounded exponentials
+    p.ws_o[slot * D + col] = (L > 0.f) ? o / Lr : 0.f;
     if (col == 0) p.ws_lse[slot] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
   }
 }

@@ -18,14 +18,17 @@
 //   warps 0-3  softmax warpgroup of tile A; warps 4-7 that of tile B.  Thread
 //              r of a warpgroup owns query row r of its tile, which is TMEM
 //              lane r.  It reads S from TMEM, masks, keeps the running max m
-//              and sum l, writes P (bf16) back into TMEM over S, rescales O
+//              and sums l (of the exponentials, for lse) and l_r (of their
+//              bf16 roundings, which divides O), writes P (bf16) back into
+//              TMEM over S, rescales O
 //              in TMEM when m grows by more than kRescaleThreshold (log2
 //              units), and writes its O row and lse in the epilogue.
 //   warp 8     TMA producer: Q tiles through a 3-buffer ring (so an item's
 //              Q_A can land while the previous item still runs), K/V copies
 //              in pairs {V_(j-1), K_j} through a 4-slot ring; an item's last
 //              V travels with the next item's K_0.
-//   warp 9     tcgen05 issuer (one thread), also owns the TMEM allocation.
+//   warp 9     tcgen05 issuer (the whole warp runs the loop, one elected
+//              lane issues), also owns the TMEM allocation.
 //              Issue order per key tile j:
 //                S_A = Q_A K_j^T,  O_B += P_B(j-1) V_(j-1),  S_B = Q_B K_j^T,
 //                O_A += P_A(j) V_j
@@ -109,26 +112,19 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return wait_slow(bar, parity, p.wait_ns, p.status, abort_flag);
 }
 
-// O (+)= P V with P (bf16, 128 x kBN) read from TMEM.
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Exponentials, packed-bf16 P and the partial row sum of one 64-key half
+// Exponentials, packed-bf16 P and the partial row sums of one 64-key half
 // (keys 64*H ..) of the score row held in sr[]; P goes to TMEM columns
-// [32*H, 32*H + 32) of S.
+// [32*H, 32*H + 32) of S.  Two sums: of the fp32 exponentials (`exact`,
+// for the log-sum-exp) and of the bf16 values the P*V product uses
+// (`rounded`, the normaliser of O, so that O is a convex combination of V
+// rows even when one weight dominates and its rounding error would
+// otherwise pass straight into the output).
 template <int H>
-__device__ __forceinline__ float softmax_exp_half(const uint32_t (&sr)[128], uint32_t t_s,
-                                                  float scale_log2, float m_use) {
+__device__ __forceinline__ void softmax_exp_half(const uint32_t (&sr)[128], uint32_t t_s, float scale_log2,
+                                                 float m_use, float& exact, float& rounded) {
   const uint64_t c2 = f2_pack(scale_log2, scale_log2);
   const uint64_t nm2 = f2_pack(-m_use, -m_use);
-  uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+  uint64_t sum2[2] = {0ull, 0ull}, sumr2[2] = {0ull, 0ull};
 #pragma unroll
   for (int h = 2 * H; h < 2 * H + 2; ++h) {
     uint32_t pk[16];
@@ -141,15 +137,17 @@ __device__ __forceinline__ float softmax_exp_half(const uint32_t (&sr)[128], uin
       f2_unpack(x2, x0, x1);
       const float p0 = ex2_approx(x0);
       const float p1 = ex2_approx(x1);
-      sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
+      sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
       pk[c] = pack_bf16x2(p0, p1);
+      sumr2[c & 1] = f2_add(sumr2[c & 1], f2_pack(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xFFFF0000u)));
     }
     tmem_st_32x32b_x16(t_s + 16 * h, pk);
   }
-  const uint64_t t2 = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
   float s0, s1;
-  f2_unpack(t2, s0, s1);
-  return s0 + s1;
+  f2_unpack(f2_add(sum2[0], sum2[1]), s0, s1);
+  exact += s0 + s1;
+  f2_unpack(f2_add(sumr2[0], sumr2[1]), s0, s1);
+  rounded += s0 + s1;
 }
 
 struct TileInfo {
@@ -316,7 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop in lockstep and one elected lane
+    // (always lane 0: every lane is active) issues each tcgen05 operation,
+    // so descriptors and counters stay warp-uniform.
+    {
       constexpr uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(kBM, D, false, true);
       // Descriptors are built once; a k-step, sub-tile, Q buffer or ring
@@ -341,19 +342,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * (kSubTileBytes / 16) + (kk % 4) * 2;
-          umma_bf16_ss(tmem + tmem_s_col(x), qd + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
+          umma_bf16_ss_warp(tmem + tmem_s_col(x), qd + off, kb + off, id_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&sm.s_full[x]);
+        umma_commit_warp(&sm.s_full[x]);
       };
       // O_X (+)= P_X V with V at vb; acc0 = 0 starts O_X afresh
       auto pv = [&](int x, uint64_t vb, uint32_t acc0) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_bf16_ts(tmem + tmem_o_col(x), tmem + tmem_s_col(x) + kk * 8, vb + kk * 128, id_pv,
-                       kk > 0 ? 1u : acc0);
+          umma_bf16_ts_warp(tmem + tmem_o_col(x), tmem + tmem_s_col(x) + kk * 8, vb + kk * 128, id_pv,
+                            kk > 0 ? 1u : acc0);
+      };
+      // every lane waits; the warp goes on only if all of them saw the phase
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, &sm.abort_flag));
       };
       auto wait_q = [&](int qb) -> bool {
-        if (!wait_or_abort(&sm.q_full[qb], q_waits[qb] & 1, p, &sm.abort_flag)) return false;
+        if (!wait_all(&sm.q_full[qb], q_waits[qb] & 1)) return false;
         ++q_waits[qb];
         tc_fence_after_sync();
         return true;
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Pair base = {previous item's last V, K_0}: already complete if a
         // previous item waited for it.
         const int base = g;
-        if (!wait_or_abort(&sm.full[base & 1], (base >> 1) & 1, p, &sm.abort_flag)) break;
+        if (!wait_all(&sm.full[base & 1], (base >> 1) & 1)) break;
         tc_fence_after_sync();
         for (int j = 0; j <= n_iter; ++j) {
           const int gk = base + j;  // pair of K_j and V_(j-1)
@@ -387,15 +392,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < nA) {
             if (j == 0 && !(ok = wait_q(qa))) break;
             qk(0, qd_a, kb);
-            if (j == nA - 1) umma_commit(&sm.q_free[qa]);  // Q_A no longer read
+            if (j == nA - 1) umma_commit_warp(&sm.q_free[qa]);  // Q_A no longer read
           }
           // ---- O_B += P_B(j-1) V_(j-1)
           if (j >= 1 && j - 1 < nB) {
-            if (!(ok = wait_or_abort(&sm.p_full[1], p_waits1 & 1, p, &sm.abort_flag))) break;
+            if (!(ok = wait_all(&sm.p_full[1], p_waits1 & 1))) break;
             ++p_waits1;
             tc_fence_after_sync();
             pv(1, vb_prev, j == 1 ? 0u : 1u);
-            if (j - 1 == nB - 1) umma_commit(&sm.o_done[1]);
+            if (j - 1 == nB - 1) umma_commit_warp(&sm.o_done[1]);
           }
           // Pair base + n_iter also carries the next item's K_0; that item
           // releases it after its S_B(0).
@@ -404,19 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < nB) {
             if (j == 0 && !(ok = wait_q(qb))) break;
             qk(1, qd_b, kb);
-            if (j == nB - 1) umma_commit(&sm.q_free[qb]);
+            if (j == nB - 1) umma_commit_warp(&sm.q_free[qb]);
           }
-          umma_commit(&sm.empty[gk & 1]);  // pair {V_(j-1), K_j} no longer read
+          umma_commit_warp(&sm.empty[gk & 1]);  // pair {V_(j-1), K_j} no longer read
           // ---- pair gk+1 = {V_j, K_(j+1)}, then O_A += P_A(j) V_j (one fence
           // after both waits)
           const int gn = gk + 1;
-          if (!(ok = wait_or_abort(&sm.full[gn & 1], (gn >> 1) & 1, p, &sm.abort_flag))) break;
+          if (!(ok = wait_all(&sm.full[gn & 1], (gn >> 1) & 1))) break;
           if (j < nA) {
-            if (!(ok = wait_or_abort(&sm.p_full[0], p_waits0 & 1, p, &sm.abort_flag))) break;
+            if (!(ok = wait_all(&sm.p_full[0], p_waits0 & 1))) break;
             ++p_waits0;
             tc_fence_after_sync();
             pv(0, vb_next, j == 0 ? 0u : 1u);
-            if (j == nA - 1) umma_commit(&sm.o_done[0]);
+            if (j == nA - 1) umma_commit_warp(&sm.o_done[0]);
           } else {
             tc_fence_after_sync();
           }
@@ -444,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_full = it.ti[x].n_full;
       const long long vis_last = static_cast<long long>(row) + p.Nk - p.Nq;  // causal: keys <= vis_last
       float m_ref = -INFINITY;  // reference max, log2 units
-      float l = 0.f;
+      float l = 0.f;            // sum of the exponentials (log-sum-exp)
+      float lr = 0.f;           // sum of their bf16 roundings (normaliser of O)
       for (int j = 0; j < n_kv; ++j) {
         if (!__all_sync(0xffffffffu, wait_or_abort(&sm.s_full[x], s_waits & 1, p, &sm.abort_flag))) {
           ok = false;
@@ -491,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // gets keys 32h.., whose own S columns were already read.  The whole
         // row is handed over at once (two 4-MMA halves with a wait between
         // them measured slower than one 8-MMA group).
-        float sum = softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use);
+        float sum = 0.f, sumr = 0.f;
+        softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use, sum, sumr);
         // Lazy rescale of O_X, placed after the first half so that half's
         // score registers are free.  O_X is complete up to key tile j-1
         // here: P*V_(j-1) was issued before S_X(j), and s_full fires only
@@ -509,8 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_32x32b_x16(t_o + c * 16, o);
           }
         }
-        sum += softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use);
+        softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use, sum, sumr);
         l = l * alpha + sum;
+        lr = lr * alpha + sumr;
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(&sm.p_full[x]);
@@ -518,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
-      // O row -> 1/l -> bf16 -> straight to global memory (16-byte stores;
+      // O row -> 1/l_r -> bf16 -> straight to global memory (16-byte stores;
       // rows past Nq are skipped), so the Q buffer is free for the next
       // item as soon as its last S has been computed.
       if (n_kv > 0) {
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
       }
       const bool row_has_keys = n_kv > 0 && l > 0.f;
-      const float inv_l = row_has_keys ? 1.f / l : 0.f;
+      const float inv_l = row_has_keys ? 1.f / lr : 0.f;
       if (p.lse != nullptr && row < p.Nq) {
         const float lse = row_has_keys ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         p.lse[static_cast<size_t>(it.zq) * p.Nq + row] = lse;
