@@ -515,16 +515,50 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
       (static_cast<long long>(B) * Hkv * Nk * d / 4 + 255) / 256 > 0x7FFFFFFFll)
     return EXATTN_ERR_UNSUPPORTED;
   if (B == 0 || (Nq == 0 && Nk == 0)) return EXATTN_OK;
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr ||
-      lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+  // the tensors of an empty side (no queries, or no keys) may be NULL
+  if ((Nq > 0 && (q == nullptr || out == nullptr || dout == nullptr || lse == nullptr || dq == nullptr)) ||
+      (Nk > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)))
     return EXATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
+  if ((Nq > 0 && (!aligned16(q) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) || !aligned4(lse))) ||
+      (Nk > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))))
     return EXATTN_ERR_ALIGNMENT;
   const size_t need = attn_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return EXATTN_ERR_WORKSPACE;
   if (need > 0 && !aligned16(workspace)) return EXATTN_ERR_ALIGNMENT;
   exattn::BwdArgs a;
+  exattn::DeviceGuard g;
+  CUtensorMap maps[8];  // copied into the launches' parameters
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev;
+    int rc = device_state(&dev, &g.status);
+    if (rc != EXATTN_OK) return rc;
+    const long long pq = static_cast<long long>(B) * Hq, pk = static_cast<long long>(B) * Hkv;
+    if (Nq > 0) {
+      if ((rc = tensor_map(dev, q, d, Nq, pq, &maps[0], 64)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, dout, d, Nq, pq, &maps[1], 64)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, q, d, Nq, pq, &maps[4], 128)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, dout, d, Nq, pq, &maps[5], 128)) != EXATTN_OK) return rc;
+    }
+    if (Nk > 0) {
+      if ((rc = tensor_map(dev, k, d, Nk, pk, &maps[2], 128)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, v, d, Nk, pk, &maps[3], 128)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, k, d, Nk, pk, &maps[6], 64)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, v, d, Nk, pk, &maps[7], 64)) != EXATTN_OK) return rc;
+    }
+    // an empty side has no tiles to load: its maps are stand-ins, never used
+    if (Nq == 0) maps[0] = maps[1] = maps[4] = maps[5] = maps[2];
+    if (Nk == 0) maps[2] = maps[3] = maps[6] = maps[7] = maps[0];
+  }
+  g.wait_ns = wait_budget_ns();
+  a.tm_q64 = &maps[0];
+  a.tm_do64 = &maps[1];
+  a.tm_k128 = &maps[2];
+  a.tm_v128 = &maps[3];
+  a.tm_q128 = &maps[4];
+  a.tm_do128 = &maps[5];
+  a.tm_k64 = &maps[6];
+  a.tm_v64 = &maps[7];
   a.q = q;
   a.k = k;
   a.v = v;
@@ -546,7 +580,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   a.d = d;
   a.causal = causal ? 1 : 0;
   a.scale = scale;
-  if (exattn::launch_bwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;
+  if (exattn::launch_bwd(a, g, static_cast<cudaStream_t>(stream)) != cudaSuccess) return EXATTN_ERR_CUDA;
   return EXATTN_OK;
 }
 

@@ -1,26 +1,34 @@
-// Attention backward for sm_103a: dQ, dK, dV from dO and the forward's
-// output O and log-sum-exp ("Kernel Fusion, Softmax, and Attention" page:
-// training runs a different schedule of the same attention equation).  With
-// P_ij = exp(s_ij - lse_i):
+// Attention backward for sm_103a on the tensor cores: dQ, dK, dV from dO and
+// the forward's output O and log-sum-exp ("Kernel Fusion, Softmax, and
+// Attention" page: training runs a different schedule of the same attention
+// equation).  With P_ij = exp(s_ij - lse_i):
 //   D_i   = sum_t dO_it O_it                (= sum_j P_ij dP_ij)
 //   dP_ij = <dO_i, v_j>,  dS_ij = P_ij (dP_ij - D_i)
 //   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,
 //   dQ_i  = scale sum_j dS_ij k_j
 // P and dS are recomputed tile by tile from Q, K and the saved LSE, never
-// stored.  Three kernels, no atomics (deterministic):
+// stored.  Kernels (no atomics, deterministic):
 //   * bwd_dsum_kernel: D per query row (one warp per row);
-//   * bwd_dkdv_kernel: one CTA per 64-key block of a KV head, 4 warps x 16
-//     keys; it walks every query head of the group and the query blocks the
-//     mask leaves, computing S^T = K Q^T and dP^T = V dO^T, then
-//     dV += P^T dO and dK += dS^T Q with P^T and dS^T turned from
-//     accumulator fragments into operand fragments in registers;
-//   * bwd_dq_kernel: one CTA per 64-row query block of a query head, 4 warps
-//     x 16 rows; it walks the key blocks the mask leaves, recomputing S and
-//     dP, and accumulates dQ += dS K.
-// Tiles are 64 rows x d bf16 in shared memory, 16-byte chunks XOR-swizzled
-// by row (conflict-free ldmatrix), filled by cp.async (rows past the end are
-// zero) and double-buffered.  The products run on mma.sync m16n8k16 (bf16 in,
-// fp32 accumulate).
+//   * bwd_tc_kernel<D, true> (dK/dV pass): a CTA holds one 128-key block of
+//     K and V in shared memory and streams the 64-row query tiles of one
+//     query head that the mask leaves through a 3-stage TMA ring.  Per tile
+//     the tensor core forms S^T = K Q^T and dP^T = V dO^T (M128 N64) into a
+//     double-buffered pair of TMEM regions; eight elementwise warps (thread =
+//     key = TMEM lane, two warps per lane quarter, one per half of the query
+//     columns) turn them into P^T and dS^T = P^T (dP^T - D), written back to
+//     TMEM as bf16 over their own fp32 columns; then dV += P^T dO and
+//     dK += dS^T Q accumulate in TMEM with A read from TMEM and dO, Q
+//     MN-major from shared memory.  One query head per KV head writes dK, dV
+//     directly; with GQA each query head writes fp32 partials that
+//     bwd_reduce_kernel sums in head order;
+//   * bwd_tc_kernel<D, false> (dQ pass): the mirror image, a CTA holds a
+//     128-row query tile of Q and dO and streams 64-key tiles of K and V:
+//     S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
+// Warp roles (320 threads): warps 0-7 elementwise, warp 8 TMA producer,
+// warp 9 tcgen05 issuer (warp-uniform loop, one elected lane issues) and
+// owner of the TMEM allocation.  Every wait is bounded; a wait that runs
+// out sets the device status word, drains what is in flight, frees TMEM and
+// returns.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -29,89 +37,395 @@
 namespace exattn {
 namespace {
 
-constexpr int kBwdRows = 64;
-constexpr int kBwdThreads = 128;
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr int kStatRows = 128;   // rows of a stationary tile (= TMEM lanes)
+constexpr int kStreamRows = 64;  // rows of a streamed tile (= columns of S, dP)
+constexpr int kStages = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kBufCol = 256;  // product buffers: 256 + 128 b; the second product at +64
+constexpr uint32_t kStatSub = kStatRows * 128;      // one 64-column sub-tile, 128 rows (16 KB)
+constexpr uint32_t kStreamSub = kStreamRows * 128;  // one 64-column sub-tile, 64 rows (8 KB)
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct alignas(1024) BwdSmem {
+  uint8_t stat[2][D / 64][kStatSub];              // K, V (dK/dV pass) or Q, dO (dQ pass)
+  uint8_t ring[kStages][2][D / 64][kStreamSub];   // Q, dO (dK/dV pass) or K, V (dQ pass)
+  uint64_t stat_full, full[kStages], empty[kStages], s_full[2], p_full[2], acc_done, fin;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
 
 struct BwdParams {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
-  const __nv_bfloat16* dout;
-  const float* lse;   // [B*Hq, Nq], natural log
-  const float* dsum;  // [B*Hq, Nq]: D
-  __nv_bfloat16* dq;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
-  float* part;  // GQA: per-query-head dK, dV partials [Hq/Hkv][B*Hkv][Nk][d] each, or null
-  int Hq, Hkv, Nq, Nk, causal;
+  const float* lse;      // [B*Hq, Nq], natural log
+  const float* dsum;     // [B*Hq, Nq]: D
+  __nv_bfloat16* out0;   // dK (dK/dV pass, one query head per KV head) or dQ
+  __nv_bfloat16* out1;   // dV (dK/dV pass, one query head per KV head)
+  float* part;           // dK/dV pass with GQA: partials [G][B*Hkv][Nk][D] of dK, then of dV
+  unsigned int* status;
+  unsigned long long wait_ns;
+  int Hq, Hkv, Nq, Nk, causal, n_bh, n_tiles;
   float scale, scale_log2;
 };
 
-template <int D>
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk) {
-  return base + static_cast<uint32_t>(row * (D * 2)) + (static_cast<uint32_t>(chunk ^ (row & 7)) << 4);
-}
-
-// Rows [row0, row0 + 64) of a [n_rows, D] bf16 matrix into a swizzled tile;
-// rows at or past n_rows read as zero (nothing is read for them).
-template <int D>
-__device__ __forceinline__ void load_tile(uint32_t sbase, const __nv_bfloat16* src, long long row0,
-                                          long long n_rows) {
-  constexpr int kChunks = D / 8;
-  for (int e = threadIdx.x; e < kBwdRows * kChunks; e += kBwdThreads) {
-    const int r = e / kChunks, c = e % kChunks;
-    const bool ok = row0 + r < n_rows;
-    const __nv_bfloat16* g = ok ? src + (row0 + r) * D + c * 8 : src;
-    cp_async16(tile_addr<D>(sbase, r, c), g, ok);
+__device__ __noinline__ bool bwd_wait_slow(uint64_t* bar, uint32_t parity, unsigned long long wait_ns,
+                                           unsigned int* status, uint32_t* abort_flag) {
+  volatile uint32_t* ab = abort_flag;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*ab) return false;
+    if (globaltimer_ns() - t0 > wait_ns) {
+      atomicOr(status, 1u);  // EXATTN_DEVICE_TIMEOUT_BIT
+      *ab = 1u;
+      return false;
+    }
   }
 }
 
-// A operand (16 rows x 16 k) from a row-major tile: rows r0.., k 16kk..
-template <int D>
-__device__ __forceinline__ void lda(uint32_t base, int r0, int kk, uint32_t (&a)[4]) {
-  const int lane = threadIdx.x & 31;
-  ldsm_x4(tile_addr<D>(base, r0 + (lane & 15), 2 * kk + (lane >> 4)), a[0], a[1], a[2], a[3]);
-}
-// B operands of two n-tiles (n0.., n0+8..) for k 16kk.. from a tile stored
-// [n][k] (row n holds the k values).
-template <int D>
-__device__ __forceinline__ void ldb_nk(uint32_t base, int n0, int kk, uint32_t (&b)[4]) {
-  const int lane = threadIdx.x & 31;
-  ldsm_x4(tile_addr<D>(base, n0 + (lane & 7) + ((lane >> 4) << 3), 2 * kk + ((lane >> 3) & 1)), b[0], b[1],
-          b[2], b[3]);
-}
-// B operands of two n-tiles (columns n0.., n0+8..) for k 16kk.. from a tile
-// stored [k][n] (row k holds the n values).
-template <int D>
-__device__ __forceinline__ void ldb_kn(uint32_t base, int n0, int kk, uint32_t (&b)[4]) {
-  const int lane = threadIdx.x & 31;
-  ldsm_x4_t(tile_addr<D>(base, 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3), (n0 >> 3) + (lane >> 4)),
-            b[0], b[1], b[2], b[3]);
+__device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const BwdParams& p, uint32_t* ab) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return bwd_wait_slow(bar, parity, p.wait_ns, p.status, ab);
 }
 
-// 16 x 64 fp32 accumulator fragments -> bf16 A operands for 4 k-steps of 16.
-__device__ __forceinline__ void acc_to_a(const float (&c)[8][4], uint32_t (&a)[4][4]) {
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    a[kk][0] = pack_bf16x2(c[2 * kk][0], c[2 * kk][1]);
-    a[kk][1] = pack_bf16x2(c[2 * kk][2], c[2 * kk][3]);
-    a[kk][2] = pack_bf16x2(c[2 * kk + 1][0], c[2 * kk + 1][1]);
-    a[kk][3] = pack_bf16x2(c[2 * kk + 1][2], c[2 * kk + 1][3]);
+// Which tiles a CTA works on.  KV: a 128-key block of one query head and the
+// 64-row query tiles [first, first + count) that see any of its keys.  Q: a
+// 128-row query tile and the 64-key tiles [0, count) that it sees.
+struct Work {
+  int bh, tile;      // (b * Hq + hq), stationary tile index
+  int splane, srow;  // stationary tensor plane and first row
+  int rplane, first, count;
+};
+
+template <bool KV>
+__device__ __forceinline__ Work work_of(int cta, const BwdParams& p) {
+  Work w;
+  w.bh = cta % p.n_bh;
+  const int hq = w.bh % p.Hq, b = w.bh / p.Hq;
+  const int kv_plane = b * p.Hkv + hq / (p.Hq / p.Hkv);
+  const long long shift = static_cast<long long>(p.Nk) - p.Nq;
+  if (KV) {
+    w.tile = cta / p.n_bh;  // key block; under the mask the first ones see the most queries
+    w.splane = kv_plane;
+    w.srow = w.tile * kStatRows;
+    w.rplane = w.bh;
+    const int n_q = (p.Nq + kStreamRows - 1) / kStreamRows;
+    int first = 0;
+    if (p.causal) {  // query rows i see key j iff j <= i + shift
+      const long long row = static_cast<long long>(w.srow) - shift;
+      first = row <= 0 ? 0 : static_cast<int>(min(row / kStreamRows, static_cast<long long>(n_q)));
+    }
+    w.first = first;
+    w.count = n_q - first;
+  } else {
+    w.tile = p.n_tiles - 1 - cta / p.n_bh;  // query tile; the last ones see the most keys
+    w.splane = w.bh;
+    w.srow = w.tile * kStatRows;
+    w.rplane = kv_plane;
+    w.first = 0;
+    int n_k = (p.Nk + kStreamRows - 1) / kStreamRows;
+    if (p.causal) {
+      const long long last = static_cast<long long>(w.srow) + kStatRows - 1 + shift;  // last key seen
+      n_k = last < 0 ? 0 : static_cast<int>(min(last / kStreamRows + 1, static_cast<long long>(n_k)));
+    }
+    w.count = n_k;
   }
+  return w;
 }
 
-// Stores a 16 x D fp32 accumulator (times mul) as bf16 rows row0.. (< n_rows).
-template <int D>
-__device__ __forceinline__ void store_rows(__nv_bfloat16* dst, long long row0, long long n_rows,
-                                           const float (&c)[D / 8][4], float mul) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+template <int D, bool KV>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1,
+                  const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
+                  const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Work w = work_of<KV>(blockIdx.x, p);
+
+  if (warp == kWarpLoad && lane == 0) {
+    tma_prefetch_desc(&tm_s0);
+    tma_prefetch_desc(&tm_s1);
+    tma_prefetch_desc(&tm_r0);
+    tma_prefetch_desc(&tm_r1);
+    mbar_init(&sm.stat_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.p_full[b], 8);
+    }
+    mbar_init(&sm.acc_done, 1);
+    mbar_init(&sm.fin, 1);
+    sm.abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+  const int n = w.count;
+
+  int loads_issued = 0;   // producer: streamed tiles issued
+  bool stat_issued = false;
+  bool mma_issued = false;
+
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      const uint64_t keep = l2_policy_evict_last();  // streamed tiles are re-read by other CTAs
+      mbar_arrive_expect_tx(&sm.stat_full, 2 * D * kStatRows * 2);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const long long row = row0 + g + 8 * h;
-    if (row >= n_rows) continue;
-    uint32_t* out = reinterpret_cast<uint32_t*>(dst + row * D);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sm.stat[0][c], &tm_s0, &sm.stat_full, c * 64, w.srow, w.splane);
+        tma_load_3d(sm.stat[1][c], &tm_s1, &sm.stat_full, c * 64, w.srow, w.splane);
+      }
+      stat_issued = true;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kStages;
+        if (i >= kStages && !bwd_wait(&sm.empty[s], ((i / kStages) - 1) & 1, p, &sm.abort_flag)) break;
+        const int row = (w.first + i) * kStreamRows;
+        mbar_arrive_expect_tx(&sm.full[s], 2 * D * kStreamRows * 2);
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) out[nt * 4 + t] = pack_bf16x2(c[nt][2 * h] * mul, c[nt][2 * h + 1] * mul);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d_hint(sm.ring[s][0][c], &tm_r0, &sm.full[s], c * 64, row, w.rplane, keep);
+          tma_load_3d_hint(sm.ring[s][1][c], &tm_r1, &sm.full[s], c * 64, row, w.rplane, keep);
+        }
+        loads_issued = i + 1;
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (n > 0) {
+      constexpr uint32_t id_prod = idesc_bf16_f32(128, kStreamRows, false, false);
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+      const uint64_t d_s0 = smem_desc(smem_u32(&sm.stat[0][0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t d_s1 = smem_desc(smem_u32(&sm.stat[1][0][0]), 16, 1024, kSwizzle128B);
+      constexpr uint32_t kStageUnits = 2 * (D / 64) * kStreamSub / 16;
+      constexpr uint32_t kSlotUnits = (D / 64) * kStreamSub / 16;
+      const uint64_t d_r_k = smem_desc(smem_u32(&sm.ring[0][0][0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t d_r_mn = smem_desc(smem_u32(&sm.ring[0][0][0][0]), kStreamSub, 1024, kSwizzle128B);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, bwd_wait(bar, parity, p, &sm.abort_flag));
+      };
+      // products of tile i (ring stage s) into buffer b
+      auto products = [&](int s, int b) {
+        const uint32_t col = kBufCol + 128u * b;
+        const uint64_t r0 = d_r_k + static_cast<uint64_t>(s * kStageUnits);
+        const uint64_t r1 = r0 + kSlotUnits;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk / 4) * (kStatSub / 16) + (kk % 4) * 2;
+          const uint32_t ob = (kk / 4) * (kStreamSub / 16) + (kk % 4) * 2;
+          umma_bf16_ss_warp(tmem + col, d_s0 + oa, r0 + ob, id_prod, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk / 4) * (kStatSub / 16) + (kk % 4) * 2;
+          const uint32_t ob = (kk / 4) * (kStreamSub / 16) + (kk % 4) * 2;
+          umma_bf16_ss_warp(tmem + col + 64, d_s1 + oa, r1 + ob, id_prod, kk > 0 ? 1u : 0u);
+        }
+        umma_commit_warp(&sm.s_full[b]);
+      };
+      // accumulations of tile i (stage s, buffer b); first = the CTA's first tile
+      auto accumulate = [&](int s, int b, bool first) {
+        const uint32_t col = kBufCol + 128u * b;
+        const uint64_t r0 = d_r_mn + static_cast<uint64_t>(s * kStageUnits);
+        const uint64_t r1 = r0 + kSlotUnits;
+#pragma unroll
+        for (int kk = 0; kk < kStreamRows / 16; ++kk) {
+          const uint32_t a_off = (kk / 2) * 32 + (kk % 2) * 8;  // packed columns of rows 16kk..
+          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+          if (KV) {
+            // dV += P^T dO, dK += dS^T Q
+            umma_bf16_ts_warp(tmem + 0, tmem + col + a_off, r1 + kk * 128, id_acc, acc);
+            umma_bf16_ts_warp(tmem + D, tmem + col + 64 + a_off, r0 + kk * 128, id_acc, acc);
+          } else {
+            // dQ += dS K
+            umma_bf16_ts_warp(tmem + 0, tmem + col + a_off, r0 + kk * 128, id_acc, acc);
+          }
+        }
+        umma_commit_warp(&sm.empty[s]);
+      };
+      bool ok = wait_all(&sm.stat_full, 0);
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i % kStages, b = i & 1;
+        if (!(ok = wait_all(&sm.full[s], (i / kStages) & 1))) break;
+        tc_fence_after_sync();
+        mma_issued = true;
+        products(s, b);
+        if (i >= 1) {
+          const int j = i - 1;
+          if (!(ok = wait_all(&sm.p_full[j & 1], (j >> 1) & 1))) break;
+          tc_fence_after_sync();
+          accumulate(j % kStages, j & 1, j == 0);
+        }
+      }
+      if (ok) {
+        const int j = n - 1;
+        if ((ok = wait_all(&sm.p_full[j & 1], (j >> 1) & 1))) {
+          tc_fence_after_sync();
+          accumulate(j % kStages, j & 1, j == 0);
+          umma_commit_warp(&sm.acc_done);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warps
+    const int quarter = warp & 3;  // TMEM lanes 32 quarter ..
+    const int half = warp >> 2;    // columns 32 half .. of the 64 streamed rows
+    const int r = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const long long shift = static_cast<long long>(p.Nk) - p.Nq;
+    const int row = w.srow + r;  // key (dK/dV pass) or query row (dQ pass) of this thread
+    const size_t lrow0 = static_cast<size_t>(w.bh) * p.Nq;
+    float row_lse2 = 0.f, row_d = 0.f;
+    if (!KV && row < p.Nq) {
+      row_lse2 = p.lse[lrow0 + row] * kLog2e;
+      row_d = p.dsum[lrow0 + row];
+    }
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int b = i & 1;
+      const int c0 = (w.first + i) * kStreamRows + half * 32;  // first streamed row of this half
+      float col_lse2 = 0.f, col_d = 0.f;  // dK/dV pass: query c0 + lane
+      if (KV && c0 + lane < p.Nq) {
+        col_lse2 = p.lse[lrow0 + c0 + lane] * kLog2e;
+        col_d = p.dsum[lrow0 + c0 + lane];
+      }
+      if (!__all_sync(0xffffffffu, bwd_wait(&sm.s_full[b], (i >> 1) & 1, p, &sm.abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t col = kBufCol + 128u * b + half * 32;
+      uint32_t sv[32], dpv[32];
+      tmem_ld_32x32b_x32(t_lane + col, sv);
+      tmem_ld_32x32b_x32(t_lane + col + 64, dpv);
+      tmem_ld_wait();
+      uint32_t pk[16], dsk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float pr[2], ds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int cc = c + e;
+          // (key, query) of this element
+          const long long key = KV ? row : c0 + cc;
+          const long long qry = KV ? c0 + cc : row;
+          const float l2 = KV ? __shfl_sync(0xffffffffu, col_lse2, cc) : row_lse2;
+          const float dd = KV ? __shfl_sync(0xffffffffu, col_d, cc) : row_d;
+          const bool vis = key < p.Nk && qry < p.Nq && (!p.causal || key <= qry + shift);
+          const float pe = vis ? ex2_approx(__uint_as_float(sv[cc]) * p.scale_log2 - l2) : 0.f;
+          pr[e] = pe;
+          ds[e] = pe * (__uint_as_float(dpv[cc]) - dd);
+        }
+        pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
+        dsk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+      }
+      // bf16 P^T (dK/dV pass) over this half's own first 16 S columns, bf16
+      // dS over its own first 16 dP columns (dK/dV pass) or S columns (dQ pass)
+      if (KV) {
+        tmem_st_32x32b_x16(t_lane + col, pk);
+        tmem_st_32x32b_x16(t_lane + col + 64, dsk);
+      } else {
+        tmem_st_32x32b_x16(t_lane + col, dsk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[b]);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) {
+      if (n > 0) {
+        if (!__all_sync(0xffffffffu, bwd_wait(&sm.acc_done, 0, p, &sm.abort_flag))) ok = false;
+        tc_fence_after_sync();
+      }
+    }
+    if (ok) {
+      constexpr int kHalf = D / 2;  // accumulator columns of this thread
+      const int col0 = half * kHalf;
+      const int n_acc = KV ? 2 : 1;
+#pragma unroll 1
+      for (int a = 0; a < n_acc; ++a) {
+        uint32_t v[kHalf];
+        if (n > 0) {
+#pragma unroll
+          for (int c = 0; c < kHalf / 32; ++c)
+            tmem_ld_32x32b_x32(t_lane + a * D + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) v[e] = 0u;
+        }
+        // dK/dV pass: a = 0 is dV, a = 1 is dK (times scale); dQ pass: dQ (times scale)
+        const float mul = (KV && a == 0) ? 1.f : p.scale;
+        const int lim = KV ? p.Nk : p.Nq;
+        if (row < lim) {
+          if (!KV || p.part == nullptr) {
+            const size_t plane = KV ? static_cast<size_t>(w.splane) : static_cast<size_t>(w.bh);
+            __nv_bfloat16* dst = (KV && a == 0) ? p.out1 : p.out0;
+            uint4* o = reinterpret_cast<uint4*>(dst + (plane * lim + row) * D + col0);
+#pragma unroll
+            for (int c = 0; c < kHalf / 8; ++c)
+              o[c] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * c]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
+          } else {
+            // fp32 partials of query head hq % G: [g][B*Hkv][Nk][D] for dK, then [G + g] for dV
+            const int G = p.Hq / p.Hkv;
+            const size_t plane_elems = static_cast<size_t>(p.n_bh / G) * p.Nk * D;
+            const int g = (w.bh % p.Hq) % G;
+            float* dst = p.part + static_cast<size_t>(a == 0 ? G + g : g) * plane_elems +
+                         (static_cast<size_t>(w.splane) * p.Nk + row) * D + col0;
+            float4* o = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int c = 0; c < kHalf / 4; ++c)
+              o[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                 __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+          }
+        }
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  const bool aborted = *reinterpret_cast<volatile uint32_t*>(&sm.abort_flag) != 0u;
+  if (aborted) {
+    // Drain what is still in flight before the CTA's memory goes away.
+    if (warp == kWarpLoad && lane == 0) {
+      if (stat_issued) mbar_wait(&sm.stat_full, 0, p.wait_ns);
+      for (int i = loads_issued - kStages; i < loads_issued; ++i)
+        if (i >= 0) mbar_wait(&sm.full[i % kStages], (i / kStages) & 1, p.wait_ns);
+    }
+    if (warp == kWarpMma && lane == 0 && mma_issued) {
+      umma_commit(&sm.fin);
+      mbar_wait(&sm.fin, 0, p.wait_ns);
+    }
+  }
+  __syncthreads();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -133,167 +447,6 @@ __global__ void __launch_bounds__(256) bwd_dsum_kernel(const __nv_bfloat16* out,
   if (lane == 0) dsum[row] = acc;
 }
 
-// ------------------------------------------------------------------ dK, dV
-// One CTA per (64-key block, query head); grid.x walks the query heads so
-// that the key blocks seen by the most query rows (the first ones under the
-// causal mask) are dispatched first.  With one query head per KV head the
-// CTA writes dK, dV; otherwise it writes its head's fp32 partials, summed in
-// head order by bwd_reduce_kernel.
-template <int D>
-__global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ float s_lse[2][kBwdRows], s_ds[2][kBwdRows];
-  constexpr uint32_t kTile = kBwdRows * D * 2;
-  const uint32_t base = smem_u32(smem);
-  const uint32_t s_k = base, s_v = base + kTile;
-  const uint32_t s_q[2] = {base + 2 * kTile, base + 4 * kTile};
-  const uint32_t s_do[2] = {base + 3 * kTile, base + 5 * kTile};
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int G = p.Hq / p.Hkv;
-  const int bhq = blockIdx.x;             // b * Hq + hq
-  const int b = bhq / p.Hq, hq = bhq % p.Hq;
-  const int bk = b * p.Hkv + hq / G;      // b * Hkv + hk
-  const long long n0 = static_cast<long long>(blockIdx.y) * kBwdRows;
-  const long long shift = static_cast<long long>(p.Nk) - p.Nq;
-  const size_t kv_off = static_cast<size_t>(bk) * p.Nk * D;
-  const size_t head = static_cast<size_t>(bhq) * p.Nq;
-  // query blocks that see any key of this block: rows i with n0 <= i + shift
-  const int n_qb = (p.Nq + kBwdRows - 1) / kBwdRows;
-  int qb_first = 0;
-  if (p.causal) {
-    const long long first_row = n0 - shift;
-    qb_first = first_row <= 0 ? 0 : static_cast<int>(first_row / kBwdRows);
-    if (qb_first > n_qb) qb_first = n_qb;
-  }
-  const int n_items = n_qb - qb_first;
-
-  auto load_item = [&](int it, int buf) {
-    const long long m0 = static_cast<long long>(qb_first + it) * kBwdRows;
-    load_tile<D>(s_q[buf], p.q + head * D, m0, p.Nq);
-    load_tile<D>(s_do[buf], p.dout + head * D, m0, p.Nq);
-    if (threadIdx.x < kBwdRows) {
-      const bool ok = m0 + threadIdx.x < p.Nq;
-      const size_t idx = ok ? head + m0 + threadIdx.x : head;
-      cp_async4(smem_u32(&s_lse[buf][threadIdx.x]), p.lse + idx, ok);
-      cp_async4(smem_u32(&s_ds[buf][threadIdx.x]), p.dsum + idx, ok);
-    }
-  };
-
-  load_tile<D>(s_k, p.k + kv_off, n0, p.Nk);
-  load_tile<D>(s_v, p.v + kv_off, n0, p.Nk);
-  if (n_items > 0) load_item(0, 0);
-  cp_async_commit();
-
-  float dk[D / 8][4], dv[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dk[i][e] = dv[i][e] = 0.f;
-  const long long key_lo = n0 + warp * 16 + g, key_hi = key_lo + 8;
-
-  for (int it = 0; it < n_items; ++it) {
-    const int buf = it & 1;
-    if (it + 1 < n_items) {
-      load_item(it + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const long long m0 = static_cast<long long>(qb_first + it) * kBwdRows;
-    // 16-query sub-blocks: S^T = K Q^T, dP^T = V dO^T for this warp's 16
-    // keys, then dV += P^T dO and dK += dS^T Q.  16 rather than 32 keeps
-    // S^T, dP^T and their bf16 fragments in 24 fewer registers next to the
-    // 128 dK/dV accumulators.
-    constexpr int kSub = 16;
-    constexpr int kNT = kSub / 8, kNP = kSub / 16;
-#pragma unroll 1
-    for (int sub = 0; sub < kBwdRows / kSub; ++sub) {
-      const int c0 = kSub * sub;
-      float st[kNT][4], dpt[kNT][4];
-#pragma unroll
-      for (int i = 0; i < kNT; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) st[i][e] = dpt[i][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t ak[4], av[4];
-        lda<D>(s_k, warp * 16, kk, ak);
-        lda<D>(s_v, warp * 16, kk, av);
-#pragma unroll
-        for (int np = 0; np < kNP; ++np) {
-          uint32_t bq[4], bd[4];
-          ldb_nk<D>(s_q[buf], c0 + 16 * np, kk, bq);
-          ldb_nk<D>(s_do[buf], c0 + 16 * np, kk, bd);
-          mma_bf16_16816(st[2 * np], ak, bq[0], bq[1]);
-          mma_bf16_16816(st[2 * np + 1], ak, bq[2], bq[3]);
-          mma_bf16_16816(dpt[2 * np], av, bd[0], bd[1]);
-          mma_bf16_16816(dpt[2 * np + 1], av, bd[2], bd[3]);
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = c0 + nt * 8 + 2 * t + (e & 1);
-          const long long key = (e < 2) ? key_lo : key_hi;
-          const long long qrow = m0 + col;
-          const bool ok = qrow < p.Nq && key < p.Nk && (!p.causal || key <= qrow + shift);
-          const float pt =
-              ok ? ex2_approx(st[nt][e] * p.scale_log2 - s_lse[buf][col] * 1.4426950408889634f) : 0.f;
-          st[nt][e] = pt;
-          dpt[nt][e] = pt * (dpt[nt][e] - s_ds[buf][col]);
-        }
-      uint32_t pa[kNP][4], da[kNP][4];
-#pragma unroll
-      for (int kk = 0; kk < kNP; ++kk) {
-        pa[kk][0] = pack_bf16x2(st[2 * kk][0], st[2 * kk][1]);
-        pa[kk][1] = pack_bf16x2(st[2 * kk][2], st[2 * kk][3]);
-        pa[kk][2] = pack_bf16x2(st[2 * kk + 1][0], st[2 * kk + 1][1]);
-        pa[kk][3] = pack_bf16x2(st[2 * kk + 1][2], st[2 * kk + 1][3]);
-        da[kk][0] = pack_bf16x2(dpt[2 * kk][0], dpt[2 * kk][1]);
-        da[kk][1] = pack_bf16x2(dpt[2 * kk][2], dpt[2 * kk][3]);
-        da[kk][2] = pack_bf16x2(dpt[2 * kk + 1][0], dpt[2 * kk + 1][1]);
-        da[kk][3] = pack_bf16x2(dpt[2 * kk + 1][2], dpt[2 * kk + 1][3]);
-      }
-#pragma unroll
-      for (int kk = 0; kk < kNP; ++kk)
-#pragma unroll
-        for (int np = 0; np < D / 16; ++np) {
-          uint32_t bd[4], bq[4];
-          ldb_kn<D>(s_do[buf], 16 * np, c0 / 16 + kk, bd);
-          ldb_kn<D>(s_q[buf], 16 * np, c0 / 16 + kk, bq);
-          mma_bf16_16816(dv[2 * np], pa[kk], bd[0], bd[1]);
-          mma_bf16_16816(dv[2 * np + 1], pa[kk], bd[2], bd[3]);
-          mma_bf16_16816(dk[2 * np], da[kk], bq[0], bq[1]);
-          mma_bf16_16816(dk[2 * np + 1], da[kk], bq[2], bq[3]);
-        }
-    }
-    __syncthreads();  // this buffer is refilled by the next prefetch
-  }
-  cp_async_wait<0>();
-  if (p.part == nullptr) {
-    store_rows<D>(p.dk + kv_off, n0 + warp * 16, p.Nk, dk, p.scale);
-    store_rows<D>(p.dv + kv_off, n0 + warp * 16, p.Nk, dv, 1.f);
-    return;
-  }
-  // fp32 partials of query head hq % G: [g][bk][Nk][D] for dK, then for dV
-  const size_t plane = static_cast<size_t>(gridDim.x / G) * p.Nk * D;  // B*Hkv*Nk*D
-  float* pk = p.part + static_cast<size_t>(hq % G) * plane + kv_off;
-  float* pv = pk + static_cast<size_t>(G) * plane;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const long long row = n0 + warp * 16 + g + 8 * h;
-    if (row >= p.Nk) continue;
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      *reinterpret_cast<float2*>(pk + row * D + nt * 8 + 2 * t) = make_float2(dk[nt][2 * h], dk[nt][2 * h + 1]);
-      *reinterpret_cast<float2*>(pv + row * D + nt * 8 + 2 * t) = make_float2(dv[nt][2 * h], dv[nt][2 * h + 1]);
-    }
-  }
-}
-
 // dK = scale * sum_g partial_g, dV = sum_g partial_g, in head order.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* part, __nv_bfloat16* dk,
@@ -312,163 +465,72 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* part, __nv
   *reinterpret_cast<uint2*>(dv + i) = make_uint2(pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
 }
 
-// ------------------------------------------------------------------ dQ
+// +1024 for manual alignment; at least 120 KB so that two CTAs never share
+// an SM (each holds all 512 TMEM columns).
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  constexpr uint32_t kTile = kBwdRows * D * 2;
-  const uint32_t base = smem_u32(smem);
-  const uint32_t s_q = base, s_do = base + kTile;
-  const uint32_t s_k[2] = {base + 2 * kTile, base + 4 * kTile};
-  const uint32_t s_v[2] = {base + 3 * kTile, base + 5 * kTile};
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  // grid.x walks the heads, grid.y the query blocks last to first: under
-  // the causal mask the last blocks see the most keys and go first
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq, hq = bh % p.Hq, hk = hq / (p.Hq / p.Hkv);
-  const long long m0 = static_cast<long long>(gridDim.y - 1 - blockIdx.y) * kBwdRows;
-  const long long shift = static_cast<long long>(p.Nk) - p.Nq;
-  const size_t q_off = static_cast<size_t>(bh) * p.Nq * D;
-  const size_t kv_off = (static_cast<size_t>(b) * p.Hkv + hk) * p.Nk * D;
-  int n_kb = (p.Nk + kBwdRows - 1) / kBwdRows;
-  if (p.causal) {
-    const long long last = m0 + kBwdRows - 1 + shift;  // last key the block's last row sees
-    n_kb = last < 0 ? 0 : (last / kBwdRows + 1 < n_kb ? static_cast<int>(last / kBwdRows + 1) : n_kb);
-  }
-  load_tile<D>(s_q, p.q + q_off, m0, p.Nq);
-  load_tile<D>(s_do, p.dout + q_off, m0, p.Nq);
-  if (n_kb > 0) {
-    load_tile<D>(s_k[0], p.k + kv_off, 0, p.Nk);
-    load_tile<D>(s_v[0], p.v + kv_off, 0, p.Nk);
-  }
-  cp_async_commit();
-
-  const long long row_lo = m0 + warp * 16 + g, row_hi = row_lo + 8;
-  const size_t li = static_cast<size_t>(bh) * p.Nq;
-  const float lse_lo = row_lo < p.Nq ? p.lse[li + row_lo] * 1.4426950408889634f : 0.f;
-  const float lse_hi = row_hi < p.Nq ? p.lse[li + row_hi] * 1.4426950408889634f : 0.f;
-  const float ds_lo = row_lo < p.Nq ? p.dsum[li + row_lo] : 0.f;
-  const float ds_hi = row_hi < p.Nq ? p.dsum[li + row_hi] : 0.f;
-
-  float dq[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dq[i][e] = 0.f;
-
-  for (int kb = 0; kb < n_kb; ++kb) {
-    const int buf = kb & 1;
-    if (kb + 1 < n_kb) {
-      load_tile<D>(s_k[buf ^ 1], p.k + kv_off, static_cast<long long>(kb + 1) * kBwdRows, p.Nk);
-      load_tile<D>(s_v[buf ^ 1], p.v + kv_off, static_cast<long long>(kb + 1) * kBwdRows, p.Nk);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    float s[8][4], dp[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[i][e] = dp[i][e] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t aq[4], ad[4];
-      lda<D>(s_q, warp * 16, kk, aq);
-      lda<D>(s_do, warp * 16, kk, ad);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t bk_[4], bv[4];
-        ldb_nk<D>(s_k[buf], 16 * np, kk, bk_);
-        ldb_nk<D>(s_v[buf], 16 * np, kk, bv);
-        mma_bf16_16816(s[2 * np], aq, bk_[0], bk_[1]);
-        mma_bf16_16816(s[2 * np + 1], aq, bk_[2], bk_[3]);
-        mma_bf16_16816(dp[2 * np], ad, bv[0], bv[1]);
-        mma_bf16_16816(dp[2 * np + 1], ad, bv[2], bv[3]);
-      }
-    }
-    const long long key0 = static_cast<long long>(kb) * kBwdRows;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const long long key = key0 + nt * 8 + 2 * t + (e & 1);
-        const long long row = (e < 2) ? row_lo : row_hi;
-        const bool ok = row < p.Nq && key < p.Nk && (!p.causal || key <= row + shift);
-        const float pv = ok ? ex2_approx(s[nt][e] * p.scale_log2 - (e < 2 ? lse_lo : lse_hi)) : 0.f;
-        s[nt][e] = pv * (dp[nt][e] - (e < 2 ? ds_lo : ds_hi));  // dS
-      }
-    uint32_t a[4][4];
-    acc_to_a(s, a);
-    // dQ += dS K (k = the 64 keys)
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-      for (int np = 0; np < D / 16; ++np) {
-        uint32_t bk_[4];
-        ldb_kn<D>(s_k[buf], 16 * np, kk, bk_);
-        mma_bf16_16816(dq[2 * np], a[kk], bk_[0], bk_[1]);
-        mma_bf16_16816(dq[2 * np + 1], a[kk], bk_[2], bk_[3]);
-      }
-    __syncthreads();  // this buffer is refilled by the next prefetch
-  }
-  cp_async_wait<0>();
-  store_rows<D>(p.dq + q_off, m0 + warp * 16, p.Nq, dq, p.scale);
+constexpr size_t bwd_smem_bytes() {
+  return sizeof(BwdSmem<D>) + 1024 < 120 * 1024 ? 120 * 1024 : sizeof(BwdSmem<D>) + 1024;
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t stream) {
   BwdParams p;
-  p.q = static_cast<const __nv_bfloat16*>(a.q);
-  p.k = static_cast<const __nv_bfloat16*>(a.k);
-  p.v = static_cast<const __nv_bfloat16*>(a.v);
-  p.dout = static_cast<const __nv_bfloat16*>(a.dout);
   p.lse = a.lse;
   p.dsum = a.dsum;
-  p.dq = static_cast<__nv_bfloat16*>(a.dq);
-  p.dk = static_cast<__nv_bfloat16*>(a.dk);
-  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.status = g.status;
+  p.wait_ns = g.wait_ns;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.Nq = a.Nq;
   p.Nk = a.Nk;
   p.causal = a.causal;
+  p.n_bh = a.B * a.Hq;
   p.scale = a.scale;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.scale_log2 = a.scale * kLog2e;
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.Nq;
   if (rows > 0) {
     bwd_dsum_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.out), p.dout, a.dsum, rows);
+        static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.dsum, rows);
   }
-  const int smem = 6 * kBwdRows * D * 2;
-  static std::atomic<int> smem_dkdv[64] = {}, smem_dq[64] = {};
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(bwd_dkdv_kernel<D>), smem, smem_dkdv);
+  constexpr int smem = static_cast<int>(bwd_smem_bytes<D>());
+  static std::atomic<int> smem_kv[64] = {}, smem_q[64] = {};
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, true>), smem, smem_kv);
   if (e != cudaSuccess) return e;
-  e = smem_limit_once(reinterpret_cast<const void*>(bwd_dq_kernel<D>), smem, smem_dq);
+  e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, false>), smem, smem_q);
   if (e != cudaSuccess) return e;
   const int G = a.Hq / a.Hkv;
-  p.part = G > 1 ? a.part : nullptr;
   if (a.Nk > 0) {
-    const dim3 g_kv(a.B * a.Hq, (a.Nk + kBwdRows - 1) / kBwdRows);
-    bwd_dkdv_kernel<D><<<g_kv, kBwdThreads, smem, stream>>>(p);
+    BwdParams pk = p;
+    pk.out0 = static_cast<__nv_bfloat16*>(a.dk);
+    pk.out1 = static_cast<__nv_bfloat16*>(a.dv);
+    pk.part = G > 1 ? a.part : nullptr;
+    pk.n_tiles = (a.Nk + kStatRows - 1) / kStatRows;
+    const long long grid = static_cast<long long>(pk.n_tiles) * pk.n_bh;
+    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
+        *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, pk);
     if (G > 1) {
       const long long n = static_cast<long long>(a.B) * a.Hkv * a.Nk * D;
       bwd_reduce_kernel<D><<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
-          a.part, p.dk, p.dv, n, G, a.scale);
+          a.part, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), n, G, a.scale);
     }
   }
   if (a.Nq > 0) {
-    const dim3 g_q(a.B * a.Hq, (a.Nq + kBwdRows - 1) / kBwdRows);
-    bwd_dq_kernel<D><<<g_q, kBwdThreads, smem, stream>>>(p);
+    BwdParams pq = p;
+    pq.out0 = static_cast<__nv_bfloat16*>(a.dq);
+    pq.out1 = nullptr;
+    pq.part = nullptr;
+    pq.n_tiles = (a.Nq + kStatRows - 1) / kStatRows;
+    const long long grid = static_cast<long long>(pq.n_tiles) * pq.n_bh;
+    bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
+        *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, pq);
   }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_bwd_d<64>(a, stream) : launch_bwd_d<128>(a, stream);
+cudaError_t launch_bwd(const BwdArgs& a, const DeviceGuard& g, cudaStream_t stream) {
+  return a.d == 64 ? launch_bwd_d<64>(a, g, stream) : launch_bwd_d<128>(a, g, stream);
 }
 
 }  // namespace exattn

@@ -116,6 +116,17 @@ struct RopeArgs {
 cudaError_t launch_rope_cache_write(const RopeArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
+  // tensor maps (3-D views (d, rows, planes), 64-column boxes, 128-byte
+  // swizzle) of q, dout (planes B*Hq) and k, v (planes B*Hkv), with 64-row
+  // and 128-row boxes
+  const CUtensorMap* tm_q64;
+  const CUtensorMap* tm_do64;
+  const CUtensorMap* tm_k128;
+  const CUtensorMap* tm_v128;
+  const CUtensorMap* tm_q128;
+  const CUtensorMap* tm_do128;
+  const CUtensorMap* tm_k64;
+  const CUtensorMap* tm_v64;
   const void* q;     // [B, Hq, Nq, d] bf16
   const void* k;     // [B, Hkv, Nk, d] bf16
   const void* v;
@@ -131,6 +142,6 @@ struct BwdArgs {
   float scale;
 };
 
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, const DeviceGuard& g, cudaStream_t stream);
 
 }  // namespace exattn

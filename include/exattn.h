@@ -197,10 +197,14 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  *   contents need not be initialised and are clobbered)
  * scale, causal (same bottom-right mask), d and the head counts as attn_fwd;
  * B*Hq, B*Hkv <= 65535 and Nq, Nk <= 65535 * 64 (EXATTN_ERR_UNSUPPORTED
- * beyond).  All tensor pointers 16-byte aligned (lse 4); no
- * output may overlap an input.  B == 0 or Nq == Nk == 0 launches nothing.
- * Up to four kernel launches on `stream` (D, dk/dv, their sum over query
- * heads when Hq > Hkv, dq); asynchronous, deterministic (no atomics).
+ * beyond).  All tensor pointers 16-byte aligned (lse 4); the tensors of an
+ * empty side may be NULL (q, out, dout, lse, dq when Nq == 0; k, v, dk, dv
+ * when Nk == 0: the other side's gradients are then zero); no output may
+ * overlap an input.  B == 0 or Nq == Nk == 0 launches nothing.
+ * Up to four kernel launches on `stream` (D, dk/dv on the tensor cores,
+ * their sum over query heads when Hq > Hkv, dq on the tensor cores);
+ * asynchronous, deterministic (no atomics).  A bounded wait inside the
+ * kernels that runs out sets EXATTN_DEVICE_TIMEOUT_BIT.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,

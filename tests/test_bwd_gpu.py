@@ -94,3 +94,26 @@ def test_rejects(env):
     lse = torch.zeros((1, 2, 8), device=dev, dtype=torch.float32)
     with pytest.raises(ex.ExattnError):
         ex.attn_bwd(x, x, x, x, x, lse)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(96, 160), (200, 130)])
+def test_unequal_lengths_full(env, Nq, Nk):
+    run(env, 84, 1, 4, 4, Nq, Nk, 64, False)
+
+
+def test_empty_sides(env):
+    """No keys: dQ = 0 (and nothing to write for dK, dV); no queries: dK = dV = 0."""
+    torch, ex, _, dev = env
+    q = to_dev(synth.normal_bf16(85, 0, (1, 2, 70, 128)), dev)
+    k0 = torch.zeros((1, 2, 0, 128), device=dev, dtype=torch.bfloat16)
+    out, lse = ex.attn_fwd(q, k0, k0)
+    dq, dk, dv = ex.attn_bwd(q, k0, k0, out, q, lse)
+    torch.cuda.synchronize()
+    assert torch.all(dq == 0).item() and dk.numel() == 0 and dv.numel() == 0
+    kv = to_dev(synth.normal_bf16(85, 1, (1, 2, 90, 128)), dev)
+    q0 = torch.zeros((1, 2, 0, 128), device=dev, dtype=torch.bfloat16)
+    lse0 = torch.zeros((1, 2, 0), device=dev, dtype=torch.float32)
+    dq, dk, dv = ex.attn_bwd(q0, kv, kv, q0, q0, lse0)
+    torch.cuda.synchronize()
+    assert torch.all(dk == 0).item() and torch.all(dv == 0).item() and dq.numel() == 0
+    assert ex.attn_get_device_status() == 0
