@@ -18,9 +18,9 @@
 //   warps 0-3  softmax warpgroup of tile A; warps 4-7 that of tile B.  Thread
 //              r of a warpgroup owns query row r of its tile, which is TMEM
 //              lane r.  It reads S from TMEM, masks, keeps the running max m
-//              and sums l (of the exponentials, for lse) and l_r (of their
-//              bf16 roundings, which divides O), writes P (bf16) back into
-//              TMEM over S, rescales O
+//              and sums l (of the exponentials, for lse) and l_r (l plus the
+//              bf16 rounding residual of each tile's largest weight, which
+//              divides O), writes P (bf16) back into TMEM over S, rescales O
 //              in TMEM when m grows by more than kRescaleThreshold (log2
 //              units), and writes its O row and lse in the epilogue.
 //   warp 8     TMA producer: Q tiles through a 3-buffer ring (so an item's
@@ -112,19 +112,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return wait_slow(bar, parity, p.wait_ns, p.status, abort_flag);
 }
 
-// Exponentials, packed-bf16 P and the partial row sums of one 64-key half
+// Exponentials, packed-bf16 P and the partial row sum of one 64-key half
 // (keys 64*H ..) of the score row held in sr[]; P goes to TMEM columns
-// [32*H, 32*H + 32) of S.  Two sums: of the fp32 exponentials (`exact`,
-// for the log-sum-exp) and of the bf16 values the P*V product uses
-// (`rounded`, the normaliser of O, so that O is a convex combination of V
-// rows even when one weight dominates and its rounding error would
-// otherwise pass straight into the output).
+// [32*H, 32*H + 32) of S.
 template <int H>
 __device__ __forceinline__ void softmax_exp_half(const uint32_t (&sr)[128], uint32_t t_s, float scale_log2,
-                                                 float m_use, float& exact, float& rounded) {
+                                                 float m_use, float& exact) {
   const uint64_t c2 = f2_pack(scale_log2, scale_log2);
   const uint64_t nm2 = f2_pack(-m_use, -m_use);
-  uint64_t sum2[2] = {0ull, 0ull}, sumr2[2] = {0ull, 0ull};
+  uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
   for (int h = 2 * H; h < 2 * H + 2; ++h) {
     uint32_t pk[16];
@@ -139,15 +135,12 @@ __device__ __forceinline__ void softmax_exp_half(const uint32_t (&sr)[128], uint
       const float p1 = ex2_approx(x1);
       sum2[c & 1] = f2_add(sum2[c & 1], f2_pack(p0, p1));
       pk[c] = pack_bf16x2(p0, p1);
-      sumr2[c & 1] = f2_add(sumr2[c & 1], f2_pack(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xFFFF0000u)));
     }
     tmem_st_32x32b_x16(t_s + 16 * h, pk);
   }
   float s0, s1;
   f2_unpack(f2_add(sum2[0], sum2[1]), s0, s1);
   exact += s0 + s1;
-  f2_unpack(f2_add(sumr2[0], sumr2[1]), s0, s1);
-  rounded += s0 + s1;
 }
 
 struct TileInfo {
@@ -450,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long vis_last = static_cast<long long>(row) + p.Nk - p.Nq;  // causal: keys <= vis_last
       float m_ref = -INFINITY;  // reference max, log2 units
       float l = 0.f;            // sum of the exponentials (log-sum-exp)
-      float lr = 0.f;           // sum of their bf16 roundings (normaliser of O)
+      float lr = 0.f;           // normaliser of O (see below)
       for (int j = 0; j < n_kv; ++j) {
         if (!__all_sync(0xffffffffu, wait_or_abort(&sm.s_full[x], s_waits & 1, p, &sm.abort_flag))) {
           ok = false;
@@ -482,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             acc[k] = max3f(acc[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 4 + k]));
-        float mx = max3f(acc[0], acc[1], fmaxf(acc[2], acc[3]));
-        mx *= p.scale_log2;
+        const float mxr = max3f(acc[0], acc[1], fmaxf(acc[2], acc[3]));  // raw scores
+        const float mx = mxr * p.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_ref + kRescaleThreshold) {
@@ -497,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // gets keys 32h.., whose own S columns were already read.  The whole
         // row is handed over at once (two 4-MMA halves with a wait between
         // them measured slower than one 8-MMA group).
-        float sum = 0.f, sumr = 0.f;
-        softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use, sum, sumr);
+        float sum = 0.f;
+        softmax_exp_half<0>(sr, t_s, p.scale_log2, m_use, sum);
         // Lazy rescale of O_X, placed after the first half so that half's
         // score registers are free.  O_X is complete up to key tile j-1
         // here: P*V_(j-1) was issued before S_X(j), and s_full fires only
@@ -516,9 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_32x32b_x16(t_o + c * 16, o);
           }
         }
-        softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use, sum, sumr);
+        softmax_exp_half<1>(sr, t_s, p.scale_log2, m_use, sum);
+        // The normaliser of O: the exact sum plus the bf16 rounding residual
+        // of the tile's largest weight (computed exactly as in the loop), the
+        // one weight that can dominate a row and carry its rounding error
+        // into O; the log-sum-exp keeps the exact sum.
+        const float pmax = ex2_approx(fmaf(mxr, p.scale_log2, -m_use));
+        const uint32_t pmax_b = pack_bf16x2(pmax, 0.f);
         l = l * alpha + sum;
-        lr = lr * alpha + sumr;
+        lr = lr * alpha + (sum + (__uint_as_float(pmax_b << 16) - pmax));
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(&sm.p_full[x]);
