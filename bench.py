@@ -173,11 +173,21 @@ def spread(ms):
             "ms_max": max(ms), "calls": len(ms)}
 
 
+def queue_ahead(torch, seconds=0.02):
+    """Keeps the GPU busy for a moment (a spin kernel, outside every timed
+    event pair) while the host enqueues the timed work behind it, so that a
+    host-side stall cannot leave the GPU idle between an event and the
+    launch it brackets."""
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(int(seconds * 2.0e9))
+
+
 def timed_calls(torch, fn, calls, flush, stream):
     """CUDA-event time (ms) of each of `calls` calls of fn on `stream`, L2
     flushed (a write larger than L2) before each, outside the events."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(calls)]
+    queue_ahead(torch)
     for e0, e1 in evs:
         flush.fill_(1)
         e0.record(stream)
@@ -315,6 +325,7 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    queue_ahead(torch)
     for i in range(args.steps):
         step(events[i])
     torch.cuda.synchronize()
@@ -348,6 +359,7 @@ def run_gpu(args):
             torch.cuda.synchronize()
             gevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                     for _ in range(args.graph_steps)]
+            queue_ahead(torch)
             for e0, e1 in gevs:
                 flush.fill_(1)
                 e0.record(stream)
@@ -555,6 +567,7 @@ def run_gpu(args):
             torch.cuda.synchronize()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(calls)]
+            queue_ahead(torch)
             for e0, e1 in evs:
                 flush.fill_(1)
                 e0.record(stream)
@@ -607,6 +620,7 @@ def run_gpu(args):
             torch.cuda.synchronize()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(calls)]
+            queue_ahead(torch)
             for e0, e1 in evs:
                 flush.fill_(1)
                 e0.record(stream)
