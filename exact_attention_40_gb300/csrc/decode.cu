@@ -8,7 +8,10 @@
 // d = 128).
 //
 // decode_split_kernel: one CTA per (sequence, kv head, group of up to 16
-//   query heads, split of kDecodeSplitTokens tokens).  Each of its warps
+//   query heads, split of SPLIT tokens).  SPLIT is kDecodeSplitTokens (512)
+//   or twice that when the grid stays several waves deep with the longer
+//   split (fewer CTAs, so less fixed per-CTA work per byte); the workspace
+//   is laid out for 512-token splits either way.  Each of its warps
 //   owns every kWarps-th block of the split and streams it through a private
 //   shared-memory ring: TMA copies each span as 64-column x 16-row boxes with
 //   the 128-byte swizzle, so ldmatrix reads are bank-conflict free.  Per
@@ -37,9 +40,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
 constexpr int kRows = 16;  // query heads per CTA (mma M)
 constexpr int kBlk = kDecodeBlockSize;
-constexpr int kBlocksPerSplit = kDecodeSplitTokens / kBlk;
-constexpr int kMaxBlocksPerWarp = (kBlocksPerSplit + kWarps - 1) / kWarps;
-static_assert(kMaxBlocksPerWarp <= 32, "block ids are staged one per lane");
+constexpr int kMaxSplit = 2 * kDecodeSplitTokens;
+static_assert((kMaxSplit / kBlk + kWarps - 1) / kWarps <= 32, "block ids are staged one per lane");
+constexpr int kMergeStride = 8;  // pad of the merge staging rows (floats): conflict-free float2 stores
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr uint32_t kBoxBytes = kBlk * 64 * 2;  // 16 tokens x 64 columns, bf16
@@ -81,7 +84,7 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int token, int col
   return base + (col8 >> 3) * kBoxBytes + token * 128 + (((col8 & 7) ^ (token & 7)) << 4);
 }
 
-template <int D>
+template <int D, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const SplitParams p) {
@@ -105,11 +108,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int max_ctx = p.max_blocks_per_seq * kBlk;
   const int ctx = clamp_ctx(__ldg(p.ctx_lens + seq), max_ctx, p.status);
-  const int n_splits = (ctx + kDecodeSplitTokens - 1) / kDecodeSplitTokens;
+  const int n_splits = (ctx + SPLIT - 1) / SPLIT;
   if (split >= n_splits) return;  // whole CTA: nothing of this sequence here
 
-  const int tok0 = split * kDecodeSplitTokens;
-  const int tok_end = min(ctx, tok0 + kDecodeSplitTokens);
+  const int tok0 = split * SPLIT;
+  const int tok_end = min(ctx, tok0 + SPLIT);
   const int blk0 = tok0 / kBlk;
   const int n_blk = (tok_end - tok0 + kBlk - 1) / kBlk;
   const int my_n = n_blk > warp ? (n_blk - warp + kWarps - 1) / kWarps : 0;
@@ -300,8 +303,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
   for (int n = 0; n < kNTiles; ++n) {
     const int col = 8 * n + 2 * t;
-    *reinterpret_cast<float2*>(&wacc[(warp * kRows + g) * D + col]) = make_float2(acc[n][0], acc[n][1]);
-    *reinterpret_cast<float2*>(&wacc[(warp * kRows + g + 8) * D + col]) =
+    *reinterpret_cast<float2*>(&wacc[(warp * kRows + g) * (D + kMergeStride) + col]) =
+        make_float2(acc[n][0], acc[n][1]);
+    *reinterpret_cast<float2*>(&wacc[(warp * kRows + g + 8) * (D + kMergeStride) + col]) =
         make_float2(acc[n][2], acc[n][3]);
   }
   __syncthreads();
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float wt = (sm.wm[w][r] == -INFINITY) ? 0.f : ex2_approx(sm.wm[w][r] - M);
         L += wt * sm.wl[w][r];
         Lr += wt * sm.wlr[w][r];
-        o += wt * wacc[(w * kRows + r) * D + col];
+        o += wt * wacc[(w * kRows + r) * (D + kMergeStride) + col];
       }
     }
     const size_t slot = (static_cast<size_t>(seq) * p.Hq + hq0 + r) * p.max_splits + split;
@@ -340,7 +344,7 @@ struct CombineParams {
   int Hq, max_blocks_per_seq, max_splits;
 };
 
-template <int D>
+template <int D, int SPLIT>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineParams p) {
   // Programmatic dependent launch: this grid may start before the split
   // kernel has finished; wait for its results here.
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const CombineParams p
   const int seq = blockIdx.y;
   const int col = threadIdx.x;
   const int ctx = clamp_ctx(__ldg(p.ctx_lens + seq), p.max_blocks_per_seq * kBlk, p.status);
-  const int n_splits = (ctx + kDecodeSplitTokens - 1) / kDecodeSplitTokens;
+  const int n_splits = (ctx + SPLIT - 1) / SPLIT;
   const size_t base = (static_cast<size_t>(seq) * p.Hq + hq) * p.max_splits;
   float M = -INFINITY;
   for (int s = 0; s < n_splits; ++s) M = fmaxf(M, p.ws_lse[base + s]);
@@ -373,9 +377,9 @@ size_t split_smem_bytes() {
   return sizeof(DecodeSmem<D>) + 1024;
 }
 
-template <int D>
-cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t stream) {
-  static_assert(sizeof(float) * kWarps * kRows * D <= sizeof(DecodeSmem<D>::ring),
+template <int D, int SPLIT>
+cudaError_t launch_ds(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t stream) {
+  static_assert(sizeof(float) * kWarps * kRows * (D + kMergeStride) <= sizeof(DecodeSmem<D>::ring),
                 "merge scratch must fit in the rings");
   SplitParams sp;
   sp.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -395,11 +399,11 @@ cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t str
   sp.scale_log2 = a.scale * kLog2e;
   const size_t smem = split_smem_bytes<D>();
   static std::atomic<int> smem_set[64] = {};
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(decode_split_kernel<D>),
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(decode_split_kernel<D, SPLIT>),
                                   static_cast<int>(smem), smem_set);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_splits, a.Hkv * sp.n_chunks, a.num_seqs);
-  decode_split_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_k, *a.tm_v, sp);
+  dim3 grid((a.max_blocks_per_seq * kBlk + SPLIT - 1) / SPLIT, a.Hkv * sp.n_chunks, a.num_seqs);
+  decode_split_kernel<D, SPLIT><<<grid, kThreads, smem, stream>>>(*a.tm_k, *a.tm_v, sp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -423,7 +427,19 @@ cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t str
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, cp);
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, SPLIT>, cp);
+}
+
+// The longer split when even it leaves at least four waves of CTAs (two
+// per SM) for the longest possible contexts.
+template <int D>
+cudaError_t launch_d(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  const long long chunks = (a.Hq / a.Hkv + kRows - 1) / kRows;
+  const long long long_splits = (static_cast<long long>(a.max_blocks_per_seq) * kBlk + kMaxSplit - 1) / kMaxSplit;
+  const long long ctas = long_splits * a.num_seqs * a.Hkv * chunks;
+  if (sms > 0 && ctas >= 8ll * sms) return launch_ds<D, kMaxSplit>(a, g, stream);
+  return launch_ds<D, kDecodeSplitTokens>(a, g, stream);
 }
 
 }  // namespace

@@ -103,8 +103,12 @@ size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_p
  *            attn_decode_workspace_bytes(...) bytes, 16-byte aligned;
  *            its contents need not be initialised and are clobbered.
  * block_size must be 16.  The key/value sweep of each sequence is cut into
- * splits of split_tokens (512) tokens; each split yields a partial output
- * and log-sum-exp, and a second kernel merges them (exact up to rounding).
+ * splits of 512 tokens, or of 1024 when num_seqs * Hkv * ceil(Hq/Hkv/16) *
+ * ceil(max_blocks_per_seq * 16 / 1024) is at least 8 * the SM count (the
+ * longer split keeps every SM busy there and costs less fixed work per
+ * byte); each split yields a partial output and log-sum-exp, and a second
+ * kernel merges them (exact up to rounding).  The workspace is sized for
+ * 512-token splits either way.
  * Two kernel launches.  num_blocks >= 1.  A ctx_len of 0 gives o = 0, lse = -inf; a
  * ctx_len above max_blocks_per_seq * block_size or a table entry outside
  * [0, num_blocks) is clamped/skipped and flagged in the device status word.
@@ -284,7 +288,8 @@ int attn_get_device_status(void* stream, int* status_out);
 /* Human-readable name of an exattn_status value (static string). */
 const char* attn_status_string(int status);
 
-/* Split size, in tokens, used by attn_decode_paged (a multiple of 16). */
+/* Split granularity, in tokens, that attn_decode_workspace_bytes sizes the
+ * workspace for (512; attn_decode_paged may use splits of twice that). */
 int attn_decode_split_tokens(void);
 
 /*
