@@ -7,11 +7,15 @@
 //   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,
 //   dQ_i  = scale sum_j dS_ij k_j
 // P and dS are recomputed tile by tile from Q, K and the saved LSE, never
-// stored.  Kernels (no atomics, deterministic):
-//   * bwd_dsum_kernel: D per query row (one warp per row);
+// stored.  Kernels (no atomics, deterministic), in launch order:
+//   * bwd_tc_kernel<D, false> (dQ pass): a CTA holds a 128-row query tile of
+//     Q, dO and O and streams 64-key tiles of K and V; its elementwise warps
+//     first form D for their rows from dO and O in shared memory and write it
+//     for the dK/dV pass; then S = Q K^T, dP = dO V^T, dS = P (dP - D),
+//     dQ += dS K;
 //   * bwd_tc_kernel<D, true> (dK/dV pass): a CTA holds one 128-key block of
 //     K and V in shared memory and streams the 64-row query tiles of one
-//     query head that the mask leaves through a 3-stage TMA ring.  Per tile
+//     query head that the mask leaves through a 4-stage TMA ring.  Per tile
 //     the tensor core forms S^T = K Q^T and dP^T = V dO^T (M128 N64) into a
 //     double-buffered pair of TMEM regions; eight elementwise warps (thread =
 //     key = TMEM lane, two warps per lane quarter, one per half of the query
@@ -20,10 +24,7 @@
 //     dK += dS^T Q accumulate in TMEM with A read from TMEM and dO, Q
 //     MN-major from shared memory.  One query head per KV head writes dK, dV
 //     directly; with GQA each query head writes fp32 partials that
-//     bwd_reduce_kernel sums in head order;
-//   * bwd_tc_kernel<D, false> (dQ pass): the mirror image, a CTA holds a
-//     128-row query tile of Q and dO and streams 64-key tiles of K and V:
-//     S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
+//     bwd_reduce_kernel sums in head order.
 // Warp roles (320 threads): warps 0-7 elementwise, warp 8 TMA producer,
 // warp 9 tcgen05 issuer (warp-uniform loop, one elected lane issues) and
 // owner of the TMEM allocation.  Every wait is bounded; a wait that runs
@@ -42,17 +43,18 @@ constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr int kStatRows = 128;   // rows of a stationary tile (= TMEM lanes)
 constexpr int kStreamRows = 64;  // rows of a streamed tile (= columns of S, dP)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBufCol = 256;  // product buffers: 256 + 128 b; the second product at +64
 constexpr uint32_t kStatSub = kStatRows * 128;      // one 64-column sub-tile, 128 rows (16 KB)
 constexpr uint32_t kStreamSub = kStreamRows * 128;  // one 64-column sub-tile, 64 rows (8 KB)
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+template <int D, bool KV>
 struct alignas(1024) BwdSmem {
   uint8_t stat[2][D / 64][kStatSub];              // K, V (dK/dV pass) or Q, dO (dQ pass)
   uint8_t ring[kStages][2][D / 64][kStreamSub];   // Q, dO (dK/dV pass) or K, V (dQ pass)
+  uint8_t otile[KV ? 1 : D / 64][KV ? 16 : kStatSub];  // dQ pass: O, for D = rowsum(dO * O)
   uint64_t stat_full, full[kStages], empty[kStages], s_full[2], p_full[2], acc_done, fin;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -60,7 +62,7 @@ struct alignas(1024) BwdSmem {
 
 struct BwdParams {
   const float* lse;      // [B*Hq, Nq], natural log
-  const float* dsum;     // [B*Hq, Nq]: D
+  float* dsum;           // [B*Hq, Nq]: D, written by the dQ pass, read by the dK/dV pass
   __nv_bfloat16* out0;   // dK (dK/dV pass, one query head per KV head) or dQ
   __nv_bfloat16* out1;   // dV (dK/dV pass, one query head per KV head)
   float* part;           // dK/dV pass with GQA: partials [G][B*Hkv][Nk][D] of dK, then of dV
@@ -141,9 +143,9 @@ template <int D, bool KV>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1,
                   const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_o, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(
+  BwdSmem<D, KV>& sm = *reinterpret_cast<BwdSmem<D, KV>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_s1);
     tma_prefetch_desc(&tm_r0);
     tma_prefetch_desc(&tm_r1);
+    if (!KV) tma_prefetch_desc(&tm_o);
     mbar_init(&sm.stat_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -185,13 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    // the dQ pass needs its tiles for D even when no key tile is left
+    if (lane == 0 && (n > 0 || !KV)) {
       const uint64_t keep = l2_policy_evict_last();  // streamed tiles are re-read by other CTAs
-      mbar_arrive_expect_tx(&sm.stat_full, 2 * D * kStatRows * 2);
+      mbar_arrive_expect_tx(&sm.stat_full, (KV ? 2 : 3) * D * kStatRows * 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(sm.stat[0][c], &tm_s0, &sm.stat_full, c * 64, w.srow, w.splane);
         tma_load_3d(sm.stat[1][c], &tm_s1, &sm.stat_full, c * 64, w.srow, w.splane);
+        if (!KV) tma_load_3d(sm.otile[c], &tm_o, &sm.stat_full, c * 64, w.srow, w.splane);
       }
       stat_issued = true;
       for (int i = 0; i < n; ++i) {
@@ -293,11 +298,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = w.srow + r;  // key (dK/dV pass) or query row (dQ pass) of this thread
     const size_t lrow0 = static_cast<size_t>(w.bh) * p.Nq;
     float row_lse2 = 0.f, row_d = 0.f;
-    if (!KV && row < p.Nq) {
-      row_lse2 = p.lse[lrow0 + row] * kLog2e;
-      row_d = p.dsum[lrow0 + row];
-    }
     bool ok = true;
+    if constexpr (!KV) {
+      // D of this thread's query row from the dO and O tiles (rows past Nq
+      // read as zero); written once, by the first half, for the dK/dV pass
+      if (row < p.Nq) row_lse2 = p.lse[lrow0 + row] * kLog2e;
+      ok = __all_sync(0xffffffffu, bwd_wait(&sm.stat_full, 0, p, &sm.abort_flag));
+      if (ok) {
+        const uint8_t* dob = &sm.stat[1][0][0];
+        const uint8_t* ob = &sm.otile[0][0];
+        float acc = 0.f;
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t off = sub * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
+            float fo[8], fd[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(ob + off), fo);
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(dob + off), fd);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(fd[e], fo[e], acc);
+          }
+        row_d = acc;
+        if (half == 0 && row < p.Nq) p.dsum[lrow0 + row] = acc;
+      }
+    }
     for (int i = 0; i < n; ++i) {
       const int b = i & 1;
       const int c0 = (w.first + i) * kStreamRows + half * 32;  // first streamed row of this half
@@ -317,24 +342,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_32x32b_x32(t_lane + col + 64, dpv);
       tmem_ld_wait();
       uint32_t pk[16], dsk[16];
+      // Is every element of this warp's 32 x 32 block visible and in range?
+      // Then no element needs a mask test.
+      const long long r_lo = w.srow + quarter * 32, r_hi = r_lo + 31;  // this warp's rows
+      const long long c_lo = c0, c_hi = c0 + 31;                       // this warp's columns
+      const bool interior = KV ? (r_hi < p.Nk && c_hi < p.Nq && (!p.causal || r_hi <= c_lo + shift))
+                               : (r_hi < p.Nq && c_hi < p.Nk && (!p.causal || c_hi <= r_lo + shift));
+      if (interior) {
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float pr[2], ds[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int cc = c + e;
-          // (key, query) of this element
-          const long long key = KV ? row : c0 + cc;
-          const long long qry = KV ? c0 + cc : row;
-          const float l2 = KV ? __shfl_sync(0xffffffffu, col_lse2, cc) : row_lse2;
-          const float dd = KV ? __shfl_sync(0xffffffffu, col_d, cc) : row_d;
-          const bool vis = key < p.Nk && qry < p.Nq && (!p.causal || key <= qry + shift);
-          const float pe = vis ? ex2_approx(__uint_as_float(sv[cc]) * p.scale_log2 - l2) : 0.f;
-          pr[e] = pe;
-          ds[e] = pe * (__uint_as_float(dpv[cc]) - dd);
+        for (int c = 0; c < 32; c += 2) {
+          const float l2a = KV ? __shfl_sync(0xffffffffu, col_lse2, c) : row_lse2;
+          const float l2b = KV ? __shfl_sync(0xffffffffu, col_lse2, c + 1) : row_lse2;
+          const float da = KV ? __shfl_sync(0xffffffffu, col_d, c) : row_d;
+          const float db = KV ? __shfl_sync(0xffffffffu, col_d, c + 1) : row_d;
+          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, f2_pack(-l2a, -l2b));
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), f2_pack(-da, -db));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), t2), d0, d1);
+          pk[c / 2] = pack_bf16x2(p0, p1);
+          dsk[c / 2] = pack_bf16x2(d0, d1);
         }
-        pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
-        dsk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pr[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cc = c + e;
+            // (key, query) of this element
+            const long long key = KV ? row : c0 + cc;
+            const long long qry = KV ? c0 + cc : row;
+            const float l2 = KV ? __shfl_sync(0xffffffffu, col_lse2, cc) : row_lse2;
+            const float dd = KV ? __shfl_sync(0xffffffffu, col_d, cc) : row_d;
+            const bool vis = key < p.Nk && qry < p.Nq && (!p.causal || key <= qry + shift);
+            const float pe = vis ? ex2_approx(__uint_as_float(sv[cc]) * p.scale_log2 - l2) : 0.f;
+            pr[e] = pe;
+            ds[e] = vis ? pe * (__uint_as_float(dpv[cc]) - dd) : 0.f;
+          }
+          pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
+          dsk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
       }
       // bf16 P^T (dK/dV pass) over this half's own first 16 S columns, bf16
       // dS over its own first 16 dP columns (dK/dV pass) or S columns (dQ pass)
@@ -429,24 +480,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------ D
-template <int D>
-__global__ void __launch_bounds__(256) bwd_dsum_kernel(const __nv_bfloat16* out, const __nv_bfloat16* dout,
-                                                       float* dsum, long long rows) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  constexpr int kPer = D / 32;  // 2 or 4 values per lane
-  const __nv_bfloat16* o = out + row * D + lane * kPer;
-  const __nv_bfloat16* g = dout + row * D + lane * kPer;
-  float acc = 0.f;
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dsum[row] = acc;
-}
-
 // dK = scale * sum_g partial_g, dV = sum_g partial_g, in head order.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* part, __nv_bfloat16* dk,
@@ -467,9 +500,9 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* part, __nv
 
 // +1024 for manual alignment; at least 120 KB so that two CTAs never share
 // an SM (each holds all 512 TMEM columns).
-template <int D>
+template <int D, bool KV>
 constexpr size_t bwd_smem_bytes() {
-  return sizeof(BwdSmem<D>) + 1024 < 120 * 1024 ? 120 * 1024 : sizeof(BwdSmem<D>) + 1024;
+  return sizeof(BwdSmem<D, KV>) + 1024 < 120 * 1024 ? 120 * 1024 : sizeof(BwdSmem<D, KV>) + 1024;
 }
 
 template <int D>
@@ -487,17 +520,24 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
   p.n_bh = a.B * a.Hq;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
-  const long long rows = static_cast<long long>(a.B) * a.Hq * a.Nq;
-  if (rows > 0) {
-    bwd_dsum_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.dsum, rows);
+  constexpr int smem_kv = static_cast<int>(bwd_smem_bytes<D, true>());
+  constexpr int smem_q = static_cast<int>(bwd_smem_bytes<D, false>());
+  static std::atomic<int> set_kv[64] = {}, set_q[64] = {};
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, true>), smem_kv, set_kv);
+  if (e != cudaSuccess) return e;
+  e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, false>), smem_q, set_q);
+  if (e != cudaSuccess) return e;
+  // dQ pass first: it writes D, which the dK/dV pass reads
+  if (a.Nq > 0) {
+    BwdParams pq = p;
+    pq.out0 = static_cast<__nv_bfloat16*>(a.dq);
+    pq.out1 = nullptr;
+    pq.part = nullptr;
+    pq.n_tiles = (a.Nq + kStatRows - 1) / kStatRows;
+    const long long grid = static_cast<long long>(pq.n_tiles) * pq.n_bh;
+    bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, smem_q, stream>>>(
+        *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, *a.tm_o128, pq);
   }
-  constexpr int smem = static_cast<int>(bwd_smem_bytes<D>());
-  static std::atomic<int> smem_kv[64] = {}, smem_q[64] = {};
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, true>), smem, smem_kv);
-  if (e != cudaSuccess) return e;
-  e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, false>), smem, smem_q);
-  if (e != cudaSuccess) return e;
   const int G = a.Hq / a.Hkv;
   if (a.Nk > 0) {
     BwdParams pk = p;
@@ -506,23 +546,13 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     pk.part = G > 1 ? a.part : nullptr;
     pk.n_tiles = (a.Nk + kStatRows - 1) / kStatRows;
     const long long grid = static_cast<long long>(pk.n_tiles) * pk.n_bh;
-    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
-        *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, pk);
+    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem_kv, stream>>>(
+        *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, *a.tm_k128, pk);
     if (G > 1) {
       const long long n = static_cast<long long>(a.B) * a.Hkv * a.Nk * D;
       bwd_reduce_kernel<D><<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
           a.part, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), n, G, a.scale);
     }
-  }
-  if (a.Nq > 0) {
-    BwdParams pq = p;
-    pq.out0 = static_cast<__nv_bfloat16*>(a.dq);
-    pq.out1 = nullptr;
-    pq.part = nullptr;
-    pq.n_tiles = (a.Nq + kStatRows - 1) / kStatRows;
-    const long long grid = static_cast<long long>(pq.n_tiles) * pq.n_bh;
-    bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
-        *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, pq);
   }
   return cudaGetLastError();
 }

@@ -127,6 +127,7 @@ struct BwdArgs {
   const CUtensorMap* tm_do128;
   const CUtensorMap* tm_k64;
   const CUtensorMap* tm_v64;
+  const CUtensorMap* tm_o128;  // out, 128-row boxes
   const void* q;     // [B, Hq, Nq, d] bf16
   const void* k;     // [B, Hkv, Nk, d] bf16
   const void* v;
