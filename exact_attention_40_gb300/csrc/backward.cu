@@ -23,7 +23,10 @@
 //     TMEM as bf16 over their own fp32 columns; then dV += P^T dO and
 //     dK += dS^T Q accumulate in TMEM with A read from TMEM and dO, Q
 //     MN-major from shared memory.  One query head per KV head writes dK, dV
-//     directly; with GQA each query head writes fp32 partials that
+//     directly; with GQA the G query heads of a KV head run as one cluster
+//     of G CTAs (G = 2, 4 or 8): each stages its dK, dV accumulators in its
+//     own shared memory and sums 128/G rows of all G over distributed shared
+//     memory, in head order; other group sizes write fp32 partials that
 //     bwd_reduce_kernel sums in head order.
 // Warp roles (320 threads): warps 0-7 elementwise, warp 8 TMA producer,
 // warp 9 tcgen05 issuer (warp-uniform loop, one elected lane issues) and
@@ -69,8 +72,16 @@ struct BwdParams {
   unsigned int* status;
   unsigned long long wait_ns;
   int Hq, Hkv, Nq, Nk, causal, n_bh, n_tiles;
+  int cluster;           // dK/dV pass: G when the G query heads of a KV head form a cluster, else 0
   float scale, scale_log2;
 };
+
+// Cluster-wide barrier: every thread of every CTA of the cluster arrives;
+// release / acquire order the shared-memory writes before it with the
+// distributed-shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 __device__ __noinline__ bool bwd_wait_slow(uint64_t* bar, uint32_t parity, unsigned long long wait_ns,
                                            unsigned int* status, uint32_t* abort_flag) {
@@ -426,7 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dK/dV pass: a = 0 is dV, a = 1 is dK (times scale); dQ pass: dQ (times scale)
         const float mul = (KV && a == 0) ? 1.f : p.scale;
         const int lim = KV ? p.Nk : p.Nq;
-        if (row < lim) {
+        if (KV && p.cluster > 0) {
+          // staged for the cluster's sum in the teardown (row stride D + 4 floats)
+          float* st = reinterpret_cast<float*>(&sm.stat[0][0][0]) + (a * kStatRows + r) * (D + 4) + col0;
+#pragma unroll
+          for (int c = 0; c < kHalf / 4; ++c)
+            *reinterpret_cast<float4*>(st + 4 * c) = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                                                 __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+        } else if (row < lim) {
           if (!KV || p.part == nullptr) {
             const size_t plane = KV ? static_cast<size_t>(w.splane) : static_cast<size_t>(w.bh);
             __nv_bfloat16* dst = (KV && a == 0) ? p.out1 : p.out0;
@@ -473,6 +491,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  if (KV && p.cluster > 0) {
+    // dK, dV of this key block: the sum over the cluster's G query heads,
+    // in head (cluster rank) order.  Rank k sums rows [128/G k, 128/G (k+1)).
+    cluster_sync_all();
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int G = p.cluster;
+    const int R = kStatRows / G;
+    const uint32_t base = smem_u32(&sm.stat[0][0][0]);
+    const int items = 2 * R * (D / 4);  // (accumulator, row, 4 columns)
+    for (int it = threadIdx.x; it < items; it += kThreads) {
+      const int c4 = it % (D / 4);
+      const int rl = (it / (D / 4)) % R;
+      const int a = it / (R * (D / 4));  // 0: dV, 1: dK
+      const int rr = static_cast<int>(rank) * R + rl;
+      const int key = w.srow + rr;
+      const uint32_t off = base + static_cast<uint32_t>(((a * kStatRows + rr) * (D + 4) + 4 * c4) * 4);
+      float x = 0.f, y = 0.f, z = 0.f, u = 0.f;
+      for (int k = 0; k < G; ++k) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(off), "r"(k));
+        float4 f;
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w) : "r"(remote) : "memory");
+        x += f.x; y += f.y; z += f.z; u += f.w;
+      }
+      if (key < p.Nk) {
+        const float mul = a == 0 ? 1.f : p.scale;
+        __nv_bfloat16* dst = a == 0 ? p.out1 : p.out0;
+        *reinterpret_cast<uint2*>(dst + (static_cast<size_t>(w.splane) * p.Nk + key) * D + 4 * c4) =
+            make_uint2(pack_bf16x2(x * mul, y * mul), pack_bf16x2(z * mul, u * mul));
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+  }
   if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after_sync();
@@ -520,6 +573,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
   p.n_bh = a.B * a.Hq;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  p.cluster = 0;
   constexpr int smem_kv = static_cast<int>(bwd_smem_bytes<D, true>());
   constexpr int smem_q = static_cast<int>(bwd_smem_bytes<D, false>());
   static std::atomic<int> set_kv[64] = {}, set_q[64] = {};
@@ -543,12 +597,33 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     BwdParams pk = p;
     pk.out0 = static_cast<__nv_bfloat16*>(a.dk);
     pk.out1 = static_cast<__nv_bfloat16*>(a.dv);
-    pk.part = G > 1 ? a.part : nullptr;
+    const bool clustered = G == 2 || G == 4 || G == 8;
+    pk.part = (G > 1 && !clustered) ? a.part : nullptr;
+    pk.cluster = clustered ? G : 0;
     pk.n_tiles = (a.Nk + kStatRows - 1) / kStatRows;
     const long long grid = static_cast<long long>(pk.n_tiles) * pk.n_bh;
-    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem_kv, stream>>>(
-        *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, *a.tm_k128, pk);
-    if (G > 1) {
+    if (clustered) {
+      // the G CTAs of a (key block, KV head) are consecutive: b * Hq + hkv * G + g
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(grid));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem_kv;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = G;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64,
+                             *a.tm_k128, pk);
+      if (e != cudaSuccess) return e;
+    } else {
+      bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem_kv, stream>>>(
+          *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, *a.tm_k128, pk);
+    }
+    if (G > 1 && !clustered) {
       const long long n = static_cast<long long>(a.B) * a.Hkv * a.Nk * D;
       bwd_reduce_kernel<D><<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
           a.part, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), n, G, a.scale);

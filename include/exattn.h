@@ -182,7 +182,8 @@ int attn_add_rms_norm(const void* x, const void* residual, const void* weight, v
 /*
  * Bytes of caller-provided device workspace attn_bwd needs: D (fp32
  * [B, Hq, Nq], rounded up to 16 bytes) and, when query heads share a KV head
- * (Hq > Hkv), fp32 dK and dV partials per query head ([2][B*Hq][Nk][d]).
+ * (Hq > Hkv), room for fp32 dK and dV partials per query head
+ * ([2][B*Hq][Nk][d]; used only when Hq / Hkv is not 2, 4 or 8).
  * Returns 0 for invalid arguments (or nothing to store).
  */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
@@ -205,9 +206,11 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  * empty side may be NULL (q, out, dout, lse, dq when Nq == 0; k, v, dk, dv
  * when Nk == 0: the other side's gradients are then zero); no output may
  * overlap an input.  B == 0 or Nq == Nk == 0 launches nothing.
- * Up to four kernel launches on `stream` (D, dk/dv on the tensor cores,
- * their sum over query heads when Hq > Hkv, dq on the tensor cores);
- * asynchronous, deterministic (no atomics).  A bounded wait inside the
+ * Two or three kernel launches on `stream`: dq (which also forms D) and
+ * dk/dv on the tensor cores; query heads that share a KV head are summed
+ * across a thread-block cluster when Hq / Hkv is 2, 4 or 8, and by a third
+ * kernel over the workspace partials for other group sizes.  Asynchronous,
+ * deterministic (no atomics; sums in head order).  A bounded wait inside the
  * kernels that runs out sets EXATTN_DEVICE_TIMEOUT_BIT.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,

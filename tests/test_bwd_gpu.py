@@ -117,3 +117,10 @@ def test_empty_sides(env):
     torch.cuda.synchronize()
     assert torch.all(dk == 0).item() and torch.all(dv == 0).item() and dq.numel() == 0
     assert ex.attn_get_device_status() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (6, 2), (2, 2)])
+def test_group_sizes(env, Hq, Hkv):
+    # groups of 8 (one cluster of 8 CTAs per key block), 3 (fp32 partials and
+    # their sum) and 1 (no reduction)
+    run(env, 86, 1, Hq, Hkv, 200, 200, 64, True)
