@@ -300,6 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sm.q[b][c], &tm_q, &sm.q_full[b], c * 64, it.m0 + x * kBM, it.zq);
           ++q_loads[b];
           ++qt;
+          if (round == 0 && x == 0) {
+            // the CTA's first S needs only K_0 and Q_A: let them arrive
+            // before the rest of the first item's copies share the bandwidth
+            if (!(ok = wait_or_abort(&sm.full[0], 0, p, &sm.abort_flag))) break;
+            if (!(ok = wait_or_abort(&sm.q_full[b], 0, p, &sm.abort_flag))) break;
+          }
         }
         for (int j = 1; ok && j < it.n_iter; ++j) ok = issue_pair(it.zk, j);
       }
