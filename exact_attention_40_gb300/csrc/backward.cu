@@ -597,7 +597,36 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     BwdParams pk = p;
     pk.out0 = static_cast<__nv_bfloat16*>(a.dk);
     pk.out1 = static_cast<__nv_bfloat16*>(a.dv);
-    const bool clustered = G == 2 || G == 4 || G == 8;
+    bool clustered = G == 2 || G == 4 || G == 8;
+    if (clustered) {
+      // the cluster shape must fit the device at least once (G SMs of one
+      // GPC with this much shared memory each); else the partial-sum path
+      static std::atomic<int> fits[64][4] = {};  // per device and G = 2, 4, 8: 0 unknown, 1 yes, 2 no
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+      const int gi = G == 2 ? 0 : (G == 4 ? 1 : 2);
+      int f = fits[dev][gi].load(std::memory_order_acquire);
+      if (f == 0) {
+        cudaLaunchConfig_t probe = {};
+        probe.gridDim = dim3(static_cast<unsigned>(G));
+        probe.blockDim = dim3(kThreads);
+        probe.dynamicSmemBytes = smem_kv;
+        cudaLaunchAttribute pa[1];
+        pa[0].id = cudaLaunchAttributeClusterDimension;
+        pa[0].val.clusterDim.x = G;
+        pa[0].val.clusterDim.y = 1;
+        pa[0].val.clusterDim.z = 1;
+        probe.attrs = pa;
+        probe.numAttrs = 1;
+        int n_clusters = 0;
+        const cudaError_t qe =
+            cudaOccupancyMaxActiveClusters(&n_clusters, bwd_tc_kernel<D, true>, &probe);
+        f = (qe == cudaSuccess && n_clusters > 0) ? 1 : 2;
+        if (qe != cudaSuccess) (void)cudaGetLastError();  // a refused query leaves no sticky error
+        fits[dev][gi].store(f, std::memory_order_release);
+      }
+      clustered = f == 1;
+    }
     pk.part = (G > 1 && !clustered) ? a.part : nullptr;
     pk.cluster = clustered ? G : 0;
     pk.n_tiles = (a.Nk + kStatRows - 1) / kStatRows;
