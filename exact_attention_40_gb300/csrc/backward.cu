@@ -8,26 +8,32 @@
 //   dQ_i  = scale sum_j dS_ij k_j
 // P and dS are recomputed tile by tile from Q, K and the saved LSE, never
 // stored.  Kernels (no atomics, deterministic), in launch order:
-//   * bwd_tc_kernel<D, false> (dQ pass): a CTA holds a 128-row query tile of
-//     Q, dO and O and streams 64-key tiles of K and V; its elementwise warps
-//     first form D for their rows from dO and O in shared memory and write it
-//     for the dK/dV pass; then S = Q K^T, dP = dO V^T, dS = P (dP - D),
-//     dQ += dS K;
-//   * bwd_tc_kernel<D, true> (dK/dV pass): a CTA holds one 128-key block of
-//     K and V in shared memory and streams the 64-row query tiles of one
-//     query head that the mask leaves through a 4-stage TMA ring.  Per tile
-//     the tensor core forms S^T = K Q^T and dP^T = V dO^T (M128 N64) into a
+//   * bwd_tc_kernel<D, false> (dQ pass): a unit is a 128-row query tile of
+//     one head.  Its Q, dO and O tiles come into shared memory; the
+//     elementwise warps form D for their rows from dO and O (written for the
+//     dK/dV pass) and copy the Q and dO rows into TMEM, where they are the A
+//     operands of S = Q K^T and dP = dO V^T (M128 N64, B = the streamed
+//     64-key K and V tiles of a 4-stage TMA ring), so the tensor core reads
+//     only the streamed tiles from shared memory.  dS = P (dP - D) goes back
+//     to TMEM as bf16 and dQ += dS K accumulates in TMEM;
+//   * bwd_tc_kernel<D, true> (dK/dV pass): a unit is a 128-key block of one
+//     query head.  K and V stay in shared memory; the 64-row query tiles of
+//     that head that the mask leaves stream through the ring.  Per tile the
+//     tensor core forms S^T = K Q^T and dP^T = V dO^T (M128 N64) into a
 //     double-buffered pair of TMEM regions; eight elementwise warps (thread =
 //     key = TMEM lane, two warps per lane quarter, one per half of the query
 //     columns) turn them into P^T and dS^T = P^T (dP^T - D), written back to
 //     TMEM as bf16 over their own fp32 columns; then dV += P^T dO and
 //     dK += dS^T Q accumulate in TMEM with A read from TMEM and dO, Q
-//     MN-major from shared memory.  One query head per KV head writes dK, dV
-//     directly; with GQA the G query heads of a KV head run as one cluster
-//     of G CTAs (G = 2, 4 or 8): each stages its dK, dV accumulators in its
-//     own shared memory and sums 128/G rows of all G over distributed shared
-//     memory, in head order; other group sizes write fp32 partials that
-//     bwd_reduce_kernel sums in head order.
+//     MN-major from shared memory.  With one query head per KV head it
+//     writes dK, dV directly; with GQA each query head writes fp32 partials
+//     that bwd_reduce_kernel sums in head order.
+// Both passes are persistent (one CTA per SM, grid = min(units, SMs)); CTA
+// c takes unit r*G + c in even rounds r and r*G + G-1-c in odd ones, units
+// numbered heaviest first under the causal mask.  A CTA's TMA ring, product
+// buffers and accumulators run on across its units: the next unit's
+// stationary tiles load while the current one drains, and its first
+// products are queued before the previous unit's epilogue is done.
 // Warp roles (320 threads): warps 0-7 elementwise, warp 8 TMA producer,
 // warp 9 tcgen05 issuer (warp-uniform loop, one elected lane issues) and
 // owner of the TMEM allocation.  Every wait is bounded; a wait that runs
@@ -49,6 +55,9 @@ constexpr int kStreamRows = 64;  // rows of a streamed tile (= columns of S, dP)
 constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBufCol = 256;  // product buffers: 256 + 128 b; the second product at +64
+// dQ pass: Q and dO of the query tile as TMEM A operands (two bf16 a column)
+// at columns 128 and 128 + d/2, between the dQ accumulator and the buffers
+constexpr uint32_t kQCol = 128;
 constexpr uint32_t kStatSub = kStatRows * 128;      // one 64-column sub-tile, 128 rows (16 KB)
 constexpr uint32_t kStreamSub = kStreamRows * 128;  // one 64-column sub-tile, 64 rows (8 KB)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -58,7 +67,8 @@ struct alignas(1024) BwdSmem {
   uint8_t stat[2][D / 64][kStatSub];              // K, V (dK/dV pass) or Q, dO (dQ pass)
   uint8_t ring[kStages][2][D / 64][kStreamSub];   // Q, dO (dK/dV pass) or K, V (dQ pass)
   uint8_t otile[KV ? 1 : D / 64][KV ? 16 : kStatSub];  // dQ pass: O, for D = rowsum(dO * O)
-  uint64_t stat_full, full[kStages], empty[kStages], s_full[2], p_full[2], acc_done, fin;
+  uint64_t stat_full, stat_free, full[kStages], empty[kStages], s_full[2], p_full[2], acc_done, acc_free, fin;
+  uint64_t a_full, a_free;  // dQ pass: Q and dO rows in TMEM
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -72,16 +82,8 @@ struct BwdParams {
   unsigned int* status;
   unsigned long long wait_ns;
   int Hq, Hkv, Nq, Nk, causal, n_bh, n_tiles;
-  int cluster;           // dK/dV pass: G when the G query heads of a KV head form a cluster, else 0
   float scale, scale_log2;
 };
-
-// Cluster-wide barrier: every thread of every CTA of the cluster arrives;
-// release / acquire order the shared-memory writes before it with the
-// distributed-shared-memory reads after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 __device__ __noinline__ bool bwd_wait_slow(uint64_t* bar, uint32_t parity, unsigned long long wait_ns,
                                            unsigned int* status, uint32_t* abort_flag) {
@@ -160,7 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Work w = work_of<KV>(blockIdx.x, p);
+  const int n_units = p.n_tiles * p.n_bh;
+  // Persistent: CTA c takes unit r*G + c (r even) or r*G + G-1-c (r odd) in
+  // round r, G = gridDim.x; units are numbered heaviest first.
+  auto unit_of = [&](int round) -> int {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return round * G + ((round & 1) ? (G - 1 - c) : c);
+  };
 
   if (warp == kWarpLoad && lane == 0) {
     tma_prefetch_desc(&tm_s0);
@@ -169,6 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_r1);
     if (!KV) tma_prefetch_desc(&tm_o);
     mbar_init(&sm.stat_full, 1);
+    // released by the MMA warp's commit after a unit's last products and,
+    // in the dQ pass, by the eight elementwise warps once D is formed
+    mbar_init(&sm.stat_free, KV ? 1 : 8);
+    mbar_init(&sm.a_full, 8);
+    mbar_init(&sm.a_free, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
@@ -178,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[b], 8);
     }
     mbar_init(&sm.acc_done, 1);
+    mbar_init(&sm.acc_free, 8);
     mbar_init(&sm.fin, 1);
     sm.abort_flag = 0u;
     fence_mbar_init();
@@ -191,113 +205,141 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const int n = w.count;
 
-  int loads_issued = 0;   // producer: streamed tiles issued
-  bool stat_issued = false;
+  int stat_loads = 0;     // producer: stationary loads issued
+  int loads_issued = 0;   // producer: streamed tiles issued (running over units)
   bool mma_issued = false;
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
-    // the dQ pass needs its tiles for D even when no key tile is left
-    if (lane == 0 && (n > 0 || !KV)) {
+    if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();  // streamed tiles are re-read by other CTAs
-      mbar_arrive_expect_tx(&sm.stat_full, (KV ? 2 : 3) * D * kStatRows * 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sm.stat[0][c], &tm_s0, &sm.stat_full, c * 64, w.srow, w.splane);
-        tma_load_3d(sm.stat[1][c], &tm_s1, &sm.stat_full, c * 64, w.srow, w.splane);
-        if (!KV) tma_load_3d(sm.otile[c], &tm_o, &sm.stat_full, c * 64, w.srow, w.splane);
-      }
-      stat_issued = true;
-      for (int i = 0; i < n; ++i) {
-        const int s = i % kStages;
-        if (i >= kStages && !bwd_wait(&sm.empty[s], ((i / kStages) - 1) & 1, p, &sm.abort_flag)) break;
-        const int row = (w.first + i) * kStreamRows;
-        mbar_arrive_expect_tx(&sm.full[s], 2 * D * kStreamRows * 2);
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int u = unit_of(round);
+        if (u >= n_units) break;
+        const Work w = work_of<KV>(u, p);
+        // the previous unit's stationary tiles must be released first
+        if (stat_loads > 0 && !(ok = bwd_wait(&sm.stat_free, (stat_loads - 1) & 1, p, &sm.abort_flag))) break;
+        mbar_arrive_expect_tx(&sm.stat_full, (KV ? 2 : 3) * D * kStatRows * 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d_hint(sm.ring[s][0][c], &tm_r0, &sm.full[s], c * 64, row, w.rplane, keep);
-          tma_load_3d_hint(sm.ring[s][1][c], &tm_r1, &sm.full[s], c * 64, row, w.rplane, keep);
+          tma_load_3d(sm.stat[0][c], &tm_s0, &sm.stat_full, c * 64, w.srow, w.splane);
+          tma_load_3d(sm.stat[1][c], &tm_s1, &sm.stat_full, c * 64, w.srow, w.splane);
+          if (!KV) tma_load_3d(sm.otile[c], &tm_o, &sm.stat_full, c * 64, w.srow, w.splane);
         }
-        loads_issued = i + 1;
+        ++stat_loads;
+        for (int i = 0; i < w.count; ++i) {
+          const int t = loads_issued;
+          const int s = t % kStages;
+          if (t >= kStages && !(ok = bwd_wait(&sm.empty[s], ((t / kStages) - 1) & 1, p, &sm.abort_flag))) break;
+          const int row = (w.first + i) * kStreamRows;
+          mbar_arrive_expect_tx(&sm.full[s], 2 * D * kStreamRows * 2);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d_hint(sm.ring[s][0][c], &tm_r0, &sm.full[s], c * 64, row, w.rplane, keep);
+            tma_load_3d_hint(sm.ring[s][1][c], &tm_r1, &sm.full[s], c * 64, row, w.rplane, keep);
+          }
+          loads_issued = t + 1;
+        }
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (n > 0) {
-      constexpr uint32_t id_prod = idesc_bf16_f32(128, kStreamRows, false, false);
-      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
-      const uint64_t d_s0 = smem_desc(smem_u32(&sm.stat[0][0][0]), 16, 1024, kSwizzle128B);
-      const uint64_t d_s1 = smem_desc(smem_u32(&sm.stat[1][0][0]), 16, 1024, kSwizzle128B);
-      constexpr uint32_t kStageUnits = 2 * (D / 64) * kStreamSub / 16;
-      constexpr uint32_t kSlotUnits = (D / 64) * kStreamSub / 16;
-      const uint64_t d_r_k = smem_desc(smem_u32(&sm.ring[0][0][0][0]), 16, 1024, kSwizzle128B);
-      const uint64_t d_r_mn = smem_desc(smem_u32(&sm.ring[0][0][0][0]), kStreamSub, 1024, kSwizzle128B);
-      auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, bwd_wait(bar, parity, p, &sm.abort_flag));
-      };
-      // products of tile i (ring stage s) into buffer b
-      auto products = [&](int s, int b) {
-        const uint32_t col = kBufCol + 128u * b;
-        const uint64_t r0 = d_r_k + static_cast<uint64_t>(s * kStageUnits);
-        const uint64_t r1 = r0 + kSlotUnits;
+    constexpr uint32_t id_prod = idesc_bf16_f32(128, kStreamRows, false, false);
+    constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+    const uint64_t d_s0 = smem_desc(smem_u32(&sm.stat[0][0][0]), 16, 1024, kSwizzle128B);
+    const uint64_t d_s1 = smem_desc(smem_u32(&sm.stat[1][0][0]), 16, 1024, kSwizzle128B);
+    constexpr uint32_t kStageUnits = 2 * (D / 64) * kStreamSub / 16;
+    constexpr uint32_t kSlotUnits = (D / 64) * kStreamSub / 16;
+    const uint64_t d_r_k = smem_desc(smem_u32(&sm.ring[0][0][0][0]), 16, 1024, kSwizzle128B);
+    const uint64_t d_r_mn = smem_desc(smem_u32(&sm.ring[0][0][0][0]), kStreamSub, 1024, kSwizzle128B);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, bwd_wait(bar, parity, p, &sm.abort_flag));
+    };
+    // products of running tile t (ring stage t % kStages) into buffer t & 1
+    auto products = [&](int t) {
+      const int s = t % kStages, b = t & 1;
+      const uint32_t col = kBufCol + 128u * b;
+      const uint64_t r0 = d_r_k + static_cast<uint64_t>(s * kStageUnits);
+      const uint64_t r1 = r0 + kSlotUnits;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk / 4) * (kStatSub / 16) + (kk % 4) * 2;
-          const uint32_t ob = (kk / 4) * (kStreamSub / 16) + (kk % 4) * 2;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t oa = (kk / 4) * (kStatSub / 16) + (kk % 4) * 2;
+        const uint32_t ob = (kk / 4) * (kStreamSub / 16) + (kk % 4) * 2;
+        if constexpr (KV)
           umma_bf16_ss_warp(tmem + col, d_s0 + oa, r0 + ob, id_prod, kk > 0 ? 1u : 0u);
-        }
+        else  // A = Q from TMEM, 16 elements = 8 columns a step
+          umma_bf16_ts_warp(tmem + col, tmem + kQCol + kk * 8, r0 + ob, id_prod, kk > 0 ? 1u : 0u);
+      }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk / 4) * (kStatSub / 16) + (kk % 4) * 2;
-          const uint32_t ob = (kk / 4) * (kStreamSub / 16) + (kk % 4) * 2;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t oa = (kk / 4) * (kStatSub / 16) + (kk % 4) * 2;
+        const uint32_t ob = (kk / 4) * (kStreamSub / 16) + (kk % 4) * 2;
+        if constexpr (KV)
           umma_bf16_ss_warp(tmem + col + 64, d_s1 + oa, r1 + ob, id_prod, kk > 0 ? 1u : 0u);
-        }
-        umma_commit_warp(&sm.s_full[b]);
-      };
-      // accumulations of tile i (stage s, buffer b); first = the CTA's first tile
-      auto accumulate = [&](int s, int b, bool first) {
-        const uint32_t col = kBufCol + 128u * b;
-        const uint64_t r0 = d_r_mn + static_cast<uint64_t>(s * kStageUnits);
-        const uint64_t r1 = r0 + kSlotUnits;
+        else  // A = dO from TMEM
+          umma_bf16_ts_warp(tmem + col + 64, tmem + kQCol + D / 2 + kk * 8, r1 + ob, id_prod, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(&sm.s_full[b]);
+    };
+    // accumulations of running tile t; first = the unit's first tile
+    auto accumulate = [&](int t, bool first) {
+      const int s = t % kStages, b = t & 1;
+      const uint32_t col = kBufCol + 128u * b;
+      const uint64_t r0 = d_r_mn + static_cast<uint64_t>(s * kStageUnits);
+      const uint64_t r1 = r0 + kSlotUnits;
 #pragma unroll
-        for (int kk = 0; kk < kStreamRows / 16; ++kk) {
-          const uint32_t a_off = (kk / 2) * 32 + (kk % 2) * 8;  // packed columns of rows 16kk..
-          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-          if (KV) {
-            // dV += P^T dO, dK += dS^T Q
-            umma_bf16_ts_warp(tmem + 0, tmem + col + a_off, r1 + kk * 128, id_acc, acc);
-            umma_bf16_ts_warp(tmem + D, tmem + col + 64 + a_off, r0 + kk * 128, id_acc, acc);
-          } else {
-            // dQ += dS K
-            umma_bf16_ts_warp(tmem + 0, tmem + col + a_off, r0 + kk * 128, id_acc, acc);
-          }
+      for (int kk = 0; kk < kStreamRows / 16; ++kk) {
+        const uint32_t a_off = (kk / 2) * 32 + (kk % 2) * 8;  // packed columns of rows 16kk..
+        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+        if (KV) {
+          // dV += P^T dO, dK += dS^T Q
+          umma_bf16_ts_warp(tmem + 0, tmem + col + a_off, r1 + kk * 128, id_acc, acc);
+          umma_bf16_ts_warp(tmem + D, tmem + col + 64 + a_off, r0 + kk * 128, id_acc, acc);
+        } else {
+          // dQ += dS K
+          umma_bf16_ts_warp(tmem + 0, tmem + col + a_off, r0 + kk * 128, id_acc, acc);
         }
-        umma_commit_warp(&sm.empty[s]);
-      };
-      bool ok = wait_all(&sm.stat_full, 0);
+      }
+      umma_commit_warp(&sm.empty[s]);
+    };
+    bool ok = true;
+    int units = 0, tiles = 0, acc_units = 0;
+    // the unit's first accumulation waits until the previous accumulators were read
+    auto accumulate_unit_tile = [&](int t, bool first) -> bool {
+      if (first && acc_units > 0 && !wait_all(&sm.acc_free, (acc_units - 1) & 1)) return false;
+      if (!wait_all(&sm.p_full[t & 1], (t >> 1) & 1)) return false;
+      tc_fence_after_sync();
+      accumulate(t, first);
+      return true;
+    };
+    for (int round = 0; ok; ++round) {
+      const int u = unit_of(round);
+      if (u >= n_units) break;
+      const int n = work_of<KV>(u, p).count;
+      // dK/dV pass: the K and V tiles in shared memory; dQ pass: the Q and dO rows in TMEM
+      if (!(ok = wait_all(KV ? &sm.stat_full : &sm.a_full, units & 1))) break;
+      tc_fence_after_sync();
       for (int i = 0; ok && i < n; ++i) {
-        const int s = i % kStages, b = i & 1;
-        if (!(ok = wait_all(&sm.full[s], (i / kStages) & 1))) break;
+        const int t = tiles + i;
+        if (!(ok = wait_all(&sm.full[t % kStages], (t / kStages) & 1))) break;
         tc_fence_after_sync();
         mma_issued = true;
-        products(s, b);
-        if (i >= 1) {
-          const int j = i - 1;
-          if (!(ok = wait_all(&sm.p_full[j & 1], (j >> 1) & 1))) break;
-          tc_fence_after_sync();
-          accumulate(j % kStages, j & 1, j == 0);
-        }
+        products(t);
+        if (i == n - 1) umma_commit_warp(KV ? &sm.stat_free : &sm.a_free);  // the stationary operands' last reader
+        if (i >= 1) ok = accumulate_unit_tile(t - 1, i == 1);
       }
-      if (ok) {
-        const int j = n - 1;
-        if ((ok = wait_all(&sm.p_full[j & 1], (j >> 1) & 1))) {
-          tc_fence_after_sync();
-          accumulate(j % kStages, j & 1, j == 0);
-          umma_commit_warp(&sm.acc_done);
-        }
+      if (!ok) break;
+      if (n == 0) {
+        umma_commit_warp(KV ? &sm.stat_free : &sm.a_free);
+      } else {
+        if (!(ok = accumulate_unit_tile(tiles + n - 1, n == 1))) break;
+        umma_commit_warp(&sm.acc_done);
+        ++acc_units;
       }
+      tiles += n;
+      ++units;
     }
   } else {
     // ------------------------------------------------------------ elementwise warps
@@ -306,170 +348,219 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const long long shift = static_cast<long long>(p.Nk) - p.Nq;
-    const int row = w.srow + r;  // key (dK/dV pass) or query row (dQ pass) of this thread
-    const size_t lrow0 = static_cast<size_t>(w.bh) * p.Nq;
-    float row_lse2 = 0.f, row_d = 0.f;
     bool ok = true;
-    if constexpr (!KV) {
-      // D of this thread's query row from the dO and O tiles (rows past Nq
-      // read as zero); written once, by the first half, for the dK/dV pass
-      if (row < p.Nq) row_lse2 = p.lse[lrow0 + row] * kLog2e;
-      ok = __all_sync(0xffffffffu, bwd_wait(&sm.stat_full, 0, p, &sm.abort_flag));
-      if (ok) {
-        const uint8_t* dob = &sm.stat[1][0][0];
-        const uint8_t* ob = &sm.otile[0][0];
-        float acc = 0.f;
+    int units = 0, tiles = 0, acc_units = 0;
+    // dQ pass, once per unit and before the previous unit's epilogue: D of
+    // this thread's query row from the dO and O tiles (rows past Nq read as
+    // zero), written by the first half for the dK/dV pass; then this half's
+    // share of the Q and dO row into the TMEM A operands, once the previous
+    // unit's products have read them.  The shared-memory tiles are released
+    // as soon as they are read, so the next unit's can load meanwhile.
+    float nxt_lse2 = 0.f, nxt_d = 0.f;
+    auto prologue = [&](int rnd, float& lse2_out, float& d_out) -> bool {
+      const Work wq = work_of<KV>(unit_of(rnd), p);
+      const int qrow = wq.srow + r;
+      const size_t l0 = static_cast<size_t>(wq.bh) * p.Nq;
+      lse2_out = qrow < p.Nq ? p.lse[l0 + qrow] * kLog2e : 0.f;
+      if (!__all_sync(0xffffffffu, bwd_wait(&sm.stat_full, rnd & 1, p, &sm.abort_flag))) return false;
+      const uint8_t* qb = &sm.stat[0][0][0];
+      const uint8_t* dob = &sm.stat[1][0][0];
+      const uint8_t* ob = &sm.otile[0][0];
+      float acc = 0.f;
 #pragma unroll
-        for (int sub = 0; sub < D / 64; ++sub)
+      for (int sub = 0; sub < D / 64; ++sub)
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t off = sub * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-            float fo[8], fd[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4*>(ob + off), fo);
-            unpack_bf16x8(*reinterpret_cast<const uint4*>(dob + off), fd);
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t off = sub * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
+          float fo[8], fd[8];
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(ob + off), fo);
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(dob + off), fd);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc = fmaf(fd[e], fo[e], acc);
-          }
-        row_d = acc;
-        if (half == 0 && row < p.Nq) p.dsum[lrow0 + row] = acc;
+          for (int e = 0; e < 8; ++e) acc = fmaf(fd[e], fo[e], acc);
+        }
+      uint32_t qv[D / 4], dv[D / 4];  // elements [half * D / 2, + D / 2) of the row, two a word
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const int cc = half * (D / 16) + c;  // 16-byte chunk of the row
+        const uint32_t off = (cc >> 3) * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + (((cc & 7) ^ (r & 7)) << 4);
+        const uint4 a = *reinterpret_cast<const uint4*>(qb + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(dob + off);
+        qv[4 * c] = a.x; qv[4 * c + 1] = a.y; qv[4 * c + 2] = a.z; qv[4 * c + 3] = a.w;
+        dv[4 * c] = b.x; dv[4 * c + 1] = b.y; dv[4 * c + 2] = b.z; dv[4 * c + 3] = b.w;
       }
-    }
-    for (int i = 0; i < n; ++i) {
-      const int b = i & 1;
-      const int c0 = (w.first + i) * kStreamRows + half * 32;  // first streamed row of this half
-      float col_lse2 = 0.f, col_d = 0.f;  // dK/dV pass: query c0 + lane
-      if (KV && c0 + lane < p.Nq) {
-        col_lse2 = p.lse[lrow0 + c0 + lane] * kLog2e;
-        col_d = p.dsum[lrow0 + c0 + lane];
-      }
-      if (!__all_sync(0xffffffffu, bwd_wait(&sm.s_full[b], (i >> 1) & 1, p, &sm.abort_flag))) {
-        ok = false;
-        break;
-      }
+      d_out = acc;
+      if (half == 0 && qrow < p.Nq) p.dsum[l0 + qrow] = acc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.stat_free);  // the Q, dO and O tiles may be reloaded
+      if (rnd > 0 && !__all_sync(0xffffffffu, bwd_wait(&sm.a_free, (rnd - 1) & 1, p, &sm.abort_flag))) return false;
       tc_fence_after_sync();
-      const uint32_t col = kBufCol + 128u * b + half * 32;
-      uint32_t sv[32], dpv[32];
-      tmem_ld_32x32b_x32(t_lane + col, sv);
-      tmem_ld_32x32b_x32(t_lane + col + 64, dpv);
-      tmem_ld_wait();
-      uint32_t pk[16], dsk[16];
-      // Is every element of this warp's 32 x 32 block visible and in range?
-      // Then no element needs a mask test.
-      const long long r_lo = w.srow + quarter * 32, r_hi = r_lo + 31;  // this warp's rows
-      const long long c_lo = c0, c_hi = c0 + 31;                       // this warp's columns
-      const bool interior = KV ? (r_hi < p.Nk && c_hi < p.Nq && (!p.causal || r_hi <= c_lo + shift))
-                               : (r_hi < p.Nq && c_hi < p.Nk && (!p.causal || c_hi <= r_lo + shift));
-      if (interior) {
-        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float l2a = KV ? __shfl_sync(0xffffffffu, col_lse2, c) : row_lse2;
-          const float l2b = KV ? __shfl_sync(0xffffffffu, col_lse2, c + 1) : row_lse2;
-          const float da = KV ? __shfl_sync(0xffffffffu, col_d, c) : row_d;
-          const float db = KV ? __shfl_sync(0xffffffffu, col_d, c + 1) : row_d;
-          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, f2_pack(-l2a, -l2b));
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), f2_pack(-da, -db));
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(p0, p1), t2), d0, d1);
-          pk[c / 2] = pack_bf16x2(p0, p1);
-          dsk[c / 2] = pack_bf16x2(d0, d1);
-        }
+      const uint32_t qc = t_lane + kQCol + static_cast<uint32_t>(half * (D / 4));
+      if constexpr (D == 128) {
+        tmem_st_32x32b_x32(qc, *reinterpret_cast<const uint32_t(*)[32]>(&qv[0]));
+        tmem_st_32x32b_x32(qc + D / 2, *reinterpret_cast<const uint32_t(*)[32]>(&dv[0]));
       } else {
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pr[2], ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cc = c + e;
-            // (key, query) of this element
-            const long long key = KV ? row : c0 + cc;
-            const long long qry = KV ? c0 + cc : row;
-            const float l2 = KV ? __shfl_sync(0xffffffffu, col_lse2, cc) : row_lse2;
-            const float dd = KV ? __shfl_sync(0xffffffffu, col_d, cc) : row_d;
-            const bool vis = key < p.Nk && qry < p.Nq && (!p.causal || key <= qry + shift);
-            const float pe = vis ? ex2_approx(__uint_as_float(sv[cc]) * p.scale_log2 - l2) : 0.f;
-            pr[e] = pe;
-            ds[e] = vis ? pe * (__uint_as_float(dpv[cc]) - dd) : 0.f;
-          }
-          pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
-          dsk[c / 2] = pack_bf16x2(ds[0], ds[1]);
-        }
-      }
-      // bf16 P^T (dK/dV pass) over this half's own first 16 S columns, bf16
-      // dS over its own first 16 dP columns (dK/dV pass) or S columns (dQ pass)
-      if (KV) {
-        tmem_st_32x32b_x16(t_lane + col, pk);
-        tmem_st_32x32b_x16(t_lane + col + 64, dsk);
-      } else {
-        tmem_st_32x32b_x16(t_lane + col, dsk);
+        tmem_st_32x32b_x16(qc, *reinterpret_cast<const uint32_t(*)[16]>(&qv[0]));
+        tmem_st_32x32b_x16(qc + D / 2, *reinterpret_cast<const uint32_t(*)[16]>(&dv[0]));
       }
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[b]);
-    }
-    // ---------------------------------------------------------- epilogue
-    if (ok) {
+      if (lane == 0) mbar_arrive(&sm.a_full);
+      return true;
+    };
+    for (int round = 0; ok; ++round) {
+      const int u = unit_of(round);
+      if (u >= n_units) break;
+      const Work w = work_of<KV>(u, p);
+      const int n = w.count;
+      const int row = w.srow + r;  // key (dK/dV pass) or query row (dQ pass) of this thread
+      const size_t lrow0 = static_cast<size_t>(w.bh) * p.Nq;
+      float row_lse2 = 0.f, row_d = 0.f;
+      if constexpr (!KV) {
+        if (round == 0 && !(ok = prologue(0, nxt_lse2, nxt_d))) break;
+        row_lse2 = nxt_lse2;
+        row_d = nxt_d;
+      }
+      for (int i = 0; i < n; ++i) {
+        const int t = tiles + i;
+        const int b = t & 1;
+        const int c0 = (w.first + i) * kStreamRows + half * 32;  // first streamed row of this half
+        float col_lse2 = 0.f, col_d = 0.f;  // dK/dV pass: query c0 + lane
+        if (KV && c0 + lane < p.Nq) {
+          col_lse2 = p.lse[lrow0 + c0 + lane] * kLog2e;
+          col_d = p.dsum[lrow0 + c0 + lane];
+        }
+        if (!__all_sync(0xffffffffu, bwd_wait(&sm.s_full[b], (t >> 1) & 1, p, &sm.abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t col = kBufCol + 128u * b + half * 32;
+        uint32_t sv[32], dpv[32];
+        tmem_ld_32x32b_x32(t_lane + col, sv);
+        tmem_ld_32x32b_x32(t_lane + col + 64, dpv);
+        tmem_ld_wait();
+        uint32_t pk[16], dsk[16];
+        // Is every element of this warp's 32 x 32 block visible and in range?
+        // Then no element needs a mask test.
+        const long long r_lo = w.srow + quarter * 32, r_hi = r_lo + 31;  // this warp's rows
+        const long long c_lo = c0, c_hi = c0 + 31;                       // this warp's columns
+        const bool interior = KV ? (r_hi < p.Nk && c_hi < p.Nq && (!p.causal || r_hi <= c_lo + shift))
+                                 : (r_hi < p.Nq && c_hi < p.Nk && (!p.causal || c_hi <= r_lo + shift));
+        if (interior) {
+          const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+  #pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float l2a = KV ? __shfl_sync(0xffffffffu, col_lse2, c) : row_lse2;
+            const float l2b = KV ? __shfl_sync(0xffffffffu, col_lse2, c + 1) : row_lse2;
+            const float da = KV ? __shfl_sync(0xffffffffu, col_d, c) : row_d;
+            const float db = KV ? __shfl_sync(0xffffffffu, col_d, c + 1) : row_d;
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, f2_pack(-l2a, -l2b));
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), f2_pack(-da, -db));
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), t2), d0, d1);
+            pk[c / 2] = pack_bf16x2(p0, p1);
+            dsk[c / 2] = pack_bf16x2(d0, d1);
+          }
+        } else {
+  #pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float pr[2], ds[2];
+  #pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int cc = c + e;
+              // (key, query) of this element
+              const long long key = KV ? row : c0 + cc;
+              const long long qry = KV ? c0 + cc : row;
+              const float l2 = KV ? __shfl_sync(0xffffffffu, col_lse2, cc) : row_lse2;
+              const float dd = KV ? __shfl_sync(0xffffffffu, col_d, cc) : row_d;
+              const bool vis = key < p.Nk && qry < p.Nq && (!p.causal || key <= qry + shift);
+              const float pe = vis ? ex2_approx(__uint_as_float(sv[cc]) * p.scale_log2 - l2) : 0.f;
+              pr[e] = pe;
+              ds[e] = vis ? pe * (__uint_as_float(dpv[cc]) - dd) : 0.f;
+            }
+            pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
+            dsk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+          }
+        }
+        // bf16 P^T (dK/dV pass) over this half's own first 16 S columns, bf16
+        // dS over its own first 16 dP columns (dK/dV pass) or S columns (dQ pass)
+        if (KV) {
+          tmem_st_32x32b_x16(t_lane + col, pk);
+          tmem_st_32x32b_x16(t_lane + col + 64, dsk);
+        } else {
+          tmem_st_32x32b_x16(t_lane + col, dsk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[b]);
+      }
+      if (!ok) break;
+      if (!KV && unit_of(round + 1) < n_units && !(ok = prologue(round + 1, nxt_lse2, nxt_d))) break;
+      // -------------------------------------------------------- epilogue
       if (n > 0) {
-        if (!__all_sync(0xffffffffu, bwd_wait(&sm.acc_done, 0, p, &sm.abort_flag))) ok = false;
+        if (!(ok = __all_sync(0xffffffffu, bwd_wait(&sm.acc_done, acc_units & 1, p, &sm.abort_flag)))) break;
         tc_fence_after_sync();
       }
-    }
-    if (ok) {
-      constexpr int kHalf = D / 2;  // accumulator columns of this thread
-      const int col0 = half * kHalf;
-      const int n_acc = KV ? 2 : 1;
+      {
+        constexpr int kHalf = D / 2;  // accumulator columns of this thread
+        const int col0 = half * kHalf;
+        constexpr int n_acc = KV ? 2 : 1;
 #pragma unroll 1
-      for (int a = 0; a < n_acc; ++a) {
-        uint32_t v[kHalf];
-        if (n > 0) {
+        for (int a = 0; a < n_acc; ++a) {
+          uint32_t v[kHalf];
+          if (n > 0) {
 #pragma unroll
-          for (int c = 0; c < kHalf / 32; ++c)
-            tmem_ld_32x32b_x32(t_lane + a * D + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < kHalf; ++e) v[e] = 0u;
-        }
-        // dK/dV pass: a = 0 is dV, a = 1 is dK (times scale); dQ pass: dQ (times scale)
-        const float mul = (KV && a == 0) ? 1.f : p.scale;
-        const int lim = KV ? p.Nk : p.Nq;
-        if (KV && p.cluster > 0) {
-          // staged for the cluster's sum in the teardown (row stride D + 4 floats)
-          float* st = reinterpret_cast<float*>(&sm.stat[0][0][0]) + (a * kStatRows + r) * (D + 4) + col0;
-#pragma unroll
-          for (int c = 0; c < kHalf / 4; ++c)
-            *reinterpret_cast<float4*>(st + 4 * c) = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                                                 __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
-        } else if (row < lim) {
-          if (!KV || p.part == nullptr) {
-            const size_t plane = KV ? static_cast<size_t>(w.splane) : static_cast<size_t>(w.bh);
-            __nv_bfloat16* dst = (KV && a == 0) ? p.out1 : p.out0;
-            uint4* o = reinterpret_cast<uint4*>(dst + (plane * lim + row) * D + col0);
-#pragma unroll
-            for (int c = 0; c < kHalf / 8; ++c)
-              o[c] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * c]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
-                                pack_bf16x2(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
-                                pack_bf16x2(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
-                                pack_bf16x2(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
+            for (int c = 0; c < kHalf / 32; ++c)
+              tmem_ld_32x32b_x32(t_lane + a * D + col0 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+            tmem_ld_wait();
+            if (a == n_acc - 1) {
+              // the accumulators may take the next unit's first products
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sm.acc_free);
+            }
           } else {
-            // fp32 partials of query head hq % G: [g][B*Hkv][Nk][D] for dK, then [G + g] for dV
-            const int G = p.Hq / p.Hkv;
-            const size_t plane_elems = static_cast<size_t>(p.n_bh / G) * p.Nk * D;
-            const int g = (w.bh % p.Hq) % G;
-            float* dst = p.part + static_cast<size_t>(a == 0 ? G + g : g) * plane_elems +
-                         (static_cast<size_t>(w.splane) * p.Nk + row) * D + col0;
-            float4* o = reinterpret_cast<float4*>(dst);
 #pragma unroll
-            for (int c = 0; c < kHalf / 4; ++c)
-              o[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                 __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+            for (int e = 0; e < kHalf; ++e) v[e] = 0u;
+          }
+          // dK/dV pass: a = 0 is dV, a = 1 is dK (times scale); dQ pass: dQ (times scale)
+          const float mul = (KV && a == 0) ? 1.f : p.scale;
+          const int lim = KV ? p.Nk : p.Nq;
+          if (row < lim) {
+            if (!KV || p.part == nullptr) {
+              const size_t plane = KV ? static_cast<size_t>(w.splane) : static_cast<size_t>(w.bh);
+              __nv_bfloat16* dst = (KV && a == 0) ? p.out1 : p.out0;
+              uint4* o = reinterpret_cast<uint4*>(dst + (plane * lim + row) * D + col0);
+#pragma unroll
+              for (int c = 0; c < kHalf / 8; ++c)
+                o[c] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * c]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
+                                  pack_bf16x2(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
+                                  pack_bf16x2(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
+                                  pack_bf16x2(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
+            } else {
+              // fp32 partials of query head hq % G: [g][B*Hkv][Nk][D] for dK, then [G + g] for dV
+              const int G = p.Hq / p.Hkv;
+              const size_t plane_elems = static_cast<size_t>(p.n_bh / G) * p.Nk * D;
+              const int g = (w.bh % p.Hq) % G;
+              float* dst = p.part + static_cast<size_t>(a == 0 ? G + g : g) * plane_elems +
+                           (static_cast<size_t>(w.splane) * p.Nk + row) * D + col0;
+              float4* o = reinterpret_cast<float4*>(dst);
+#pragma unroll
+              for (int c = 0; c < kHalf / 4; ++c)
+                o[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                   __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+            }
           }
         }
       }
+      if (n > 0) ++acc_units;
+      tiles += n;
+      ++units;
     }
     tc_fence_before_sync();
   }
@@ -481,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (aborted) {
     // Drain what is still in flight before the CTA's memory goes away.
     if (warp == kWarpLoad && lane == 0) {
-      if (stat_issued) mbar_wait(&sm.stat_full, 0, p.wait_ns);
-      for (int i = loads_issued - kStages; i < loads_issued; ++i)
-        if (i >= 0) mbar_wait(&sm.full[i % kStages], (i / kStages) & 1, p.wait_ns);
+      if (stat_loads > 0) mbar_wait(&sm.stat_full, (stat_loads - 1) & 1, p.wait_ns);
+      for (int t = loads_issued - kStages; t < loads_issued; ++t)
+        if (t >= 0) mbar_wait(&sm.full[t % kStages], (t / kStages) & 1, p.wait_ns);
     }
     if (warp == kWarpMma && lane == 0 && mma_issued) {
       umma_commit(&sm.fin);
@@ -491,41 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if (KV && p.cluster > 0) {
-    // dK, dV of this key block: the sum over the cluster's G query heads,
-    // in head (cluster rank) order.  Rank k sums rows [128/G k, 128/G (k+1)).
-    cluster_sync_all();
-    uint32_t rank;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-    const int G = p.cluster;
-    const int R = kStatRows / G;
-    const uint32_t base = smem_u32(&sm.stat[0][0][0]);
-    const int items = 2 * R * (D / 4);  // (accumulator, row, 4 columns)
-    for (int it = threadIdx.x; it < items; it += kThreads) {
-      const int c4 = it % (D / 4);
-      const int rl = (it / (D / 4)) % R;
-      const int a = it / (R * (D / 4));  // 0: dV, 1: dK
-      const int rr = static_cast<int>(rank) * R + rl;
-      const int key = w.srow + rr;
-      const uint32_t off = base + static_cast<uint32_t>(((a * kStatRows + rr) * (D + 4) + 4 * c4) * 4);
-      float x = 0.f, y = 0.f, z = 0.f, u = 0.f;
-      for (int k = 0; k < G; ++k) {
-        uint32_t remote;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(off), "r"(k));
-        float4 f;
-        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w) : "r"(remote) : "memory");
-        x += f.x; y += f.y; z += f.z; u += f.w;
-      }
-      if (key < p.Nk) {
-        const float mul = a == 0 ? 1.f : p.scale;
-        __nv_bfloat16* dst = a == 0 ? p.out1 : p.out0;
-        *reinterpret_cast<uint2*>(dst + (static_cast<size_t>(w.splane) * p.Nk + key) * D + 4 * c4) =
-            make_uint2(pack_bf16x2(x * mul, y * mul), pack_bf16x2(z * mul, u * mul));
-      }
-    }
-    cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
-  }
   if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after_sync();
@@ -573,7 +629,6 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
   p.n_bh = a.B * a.Hq;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
-  p.cluster = 0;
   constexpr int smem_kv = static_cast<int>(bwd_smem_bytes<D, true>());
   constexpr int smem_q = static_cast<int>(bwd_smem_bytes<D, false>());
   static std::atomic<int> set_kv[64] = {}, set_q[64] = {};
@@ -581,6 +636,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
   if (e != cudaSuccess) return e;
   e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, false>), smem_q, set_q);
   if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   // dQ pass first: it writes D, which the dK/dV pass reads
   if (a.Nq > 0) {
     BwdParams pq = p;
@@ -588,7 +645,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     pq.out1 = nullptr;
     pq.part = nullptr;
     pq.n_tiles = (a.Nq + kStatRows - 1) / kStatRows;
-    const long long grid = static_cast<long long>(pq.n_tiles) * pq.n_bh;
+    const long long units = static_cast<long long>(pq.n_tiles) * pq.n_bh;
+    const long long grid = units < sms ? units : sms;
     bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, smem_q, stream>>>(
         *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, *a.tm_o128, pq);
   }
@@ -597,62 +655,13 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     BwdParams pk = p;
     pk.out0 = static_cast<__nv_bfloat16*>(a.dk);
     pk.out1 = static_cast<__nv_bfloat16*>(a.dv);
-    bool clustered = G == 2 || G == 4 || G == 8;
-    if (clustered) {
-      // the cluster shape must fit the device at least once (G SMs of one
-      // GPC with this much shared memory each); else the partial-sum path
-      static std::atomic<int> fits[64][4] = {};  // per device and G = 2, 4, 8: 0 unknown, 1 yes, 2 no
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-      const int gi = G == 2 ? 0 : (G == 4 ? 1 : 2);
-      int f = fits[dev][gi].load(std::memory_order_acquire);
-      if (f == 0) {
-        cudaLaunchConfig_t probe = {};
-        probe.gridDim = dim3(static_cast<unsigned>(G));
-        probe.blockDim = dim3(kThreads);
-        probe.dynamicSmemBytes = smem_kv;
-        cudaLaunchAttribute pa[1];
-        pa[0].id = cudaLaunchAttributeClusterDimension;
-        pa[0].val.clusterDim.x = G;
-        pa[0].val.clusterDim.y = 1;
-        pa[0].val.clusterDim.z = 1;
-        probe.attrs = pa;
-        probe.numAttrs = 1;
-        int n_clusters = 0;
-        const cudaError_t qe =
-            cudaOccupancyMaxActiveClusters(&n_clusters, bwd_tc_kernel<D, true>, &probe);
-        f = (qe == cudaSuccess && n_clusters > 0) ? 1 : 2;
-        if (qe != cudaSuccess) (void)cudaGetLastError();  // a refused query leaves no sticky error
-        fits[dev][gi].store(f, std::memory_order_release);
-      }
-      clustered = f == 1;
-    }
-    pk.part = (G > 1 && !clustered) ? a.part : nullptr;
-    pk.cluster = clustered ? G : 0;
+    pk.part = G > 1 ? a.part : nullptr;
     pk.n_tiles = (a.Nk + kStatRows - 1) / kStatRows;
-    const long long grid = static_cast<long long>(pk.n_tiles) * pk.n_bh;
-    if (clustered) {
-      // the G CTAs of a (key block, KV head) are consecutive: b * Hq + hkv * G + g
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(grid));
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = smem_kv;
-      cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = G;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64,
-                             *a.tm_k128, pk);
-      if (e != cudaSuccess) return e;
-    } else {
-      bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem_kv, stream>>>(
-          *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, *a.tm_k128, pk);
-    }
-    if (G > 1 && !clustered) {
+    const long long units = static_cast<long long>(pk.n_tiles) * pk.n_bh;
+    const long long grid = units < sms ? units : sms;
+    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem_kv, stream>>>(
+        *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, *a.tm_k128, pk);
+    if (G > 1) {
       const long long n = static_cast<long long>(a.B) * a.Hkv * a.Nk * D;
       bwd_reduce_kernel<D><<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
           a.part, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), n, G, a.scale);

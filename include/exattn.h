@@ -183,7 +183,7 @@ int attn_add_rms_norm(const void* x, const void* residual, const void* weight, v
  * Bytes of caller-provided device workspace attn_bwd needs: D (fp32
  * [B, Hq, Nq], rounded up to 16 bytes) and, when query heads share a KV head
  * (Hq > Hkv), room for fp32 dK and dV partials per query head
- * ([2][B*Hq][Nk][d]; used only when Hq / Hkv is not 2, 4 or 8).
+ * ([2][B*Hq][Nk][d]).
  * Returns 0 for invalid arguments (or nothing to store).
  */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
@@ -207,9 +207,9 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  * when Nk == 0: the other side's gradients are then zero); no output may
  * overlap an input.  B == 0 or Nq == Nk == 0 launches nothing.
  * Two or three kernel launches on `stream`: dq (which also forms D) and
- * dk/dv on the tensor cores; query heads that share a KV head are summed
- * across a thread-block cluster when Hq / Hkv is 2, 4 or 8, and by a third
- * kernel over the workspace partials for other group sizes.  Asynchronous,
+ * dk/dv on the tensor cores, each a persistent grid of at most one CTA per
+ * SM; when query heads share a KV head, each writes fp32 partials to the
+ * workspace and a third kernel sums them.  Asynchronous,
  * deterministic (no atomics; sums in head order).  A bounded wait inside the
  * kernels that runs out sets EXATTN_DEVICE_TIMEOUT_BIT.
  */

@@ -121,6 +121,6 @@ def test_empty_sides(env):
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 1), (6, 2), (2, 2)])
 def test_group_sizes(env, Hq, Hkv):
-    # groups of 8 (one cluster of 8 CTAs per key block), 3 (fp32 partials and
-    # their sum) and 1 (no reduction)
+    # groups of 8 and 3 (fp32 partials and their sum in head order) and 1
+    # (dK, dV written directly)
     run(env, 86, 1, Hq, Hkv, 200, 200, 64, True)
