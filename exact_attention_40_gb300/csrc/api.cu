@@ -179,7 +179,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
 
   exattn::PrefillArgs a;
   exattn::DeviceGuard g;
-  CUtensorMap map_q, map_k, map_v;  // copied into the launch's parameters
+  CUtensorMap map_q, map_k, map_v, map_o;  // copied into the launch's parameters
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
@@ -187,7 +187,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
     if (rc != EXATTN_OK) return rc;
     const long long pq = static_cast<long long>(B) * Hq, pk = static_cast<long long>(B) * Hkv;
     if ((rc = tensor_map(dev, q, d, Nq, pq, &map_q)) != EXATTN_OK) return rc;
+    if ((rc = tensor_map(dev, out, d, Nq, pq, &map_o)) != EXATTN_OK) return rc;
     a.tm_q = &map_q;
+    a.tm_o = &map_o;
     if (Nk > 0) {
       if ((rc = tensor_map(dev, k, d, Nk, pk, &map_k)) != EXATTN_OK) return rc;
       if ((rc = tensor_map(dev, v, d, Nk, pk, &map_v)) != EXATTN_OK) return rc;

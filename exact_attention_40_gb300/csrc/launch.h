@@ -49,7 +49,8 @@ struct PrefillArgs {
   const CUtensorMap* tm_q;
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
-  void* out;  // [B, Hq, Nq, d] bf16, written with plain 16-byte stores
+  const CUtensorMap* tm_o;  // out, stored one 128-row tile at a time with TMA
+  void* out;  // [B, Hq, Nq, d] bf16
   float* lse;
   int B, Hq, Hkv, Nq, Nk, d;
   int causal;

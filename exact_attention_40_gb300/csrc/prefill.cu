@@ -12,7 +12,7 @@
 // share every K/V tile load.  Items are numbered heaviest first and dealt in
 // a snake order so heavy and light items pair up under the causal mask; the
 // next item's Q copy and first S = Q K^T overlap the previous item's
-// epilogue.
+// epilogue, whose O tile leaves through one TMA store.
 //
 // Warp roles (320 threads):
 //   warps 0-3  softmax warpgroup of tile A; warps 4-7 that of tile B.  Thread
@@ -22,11 +22,12 @@
 //              bf16 rounding residual of each tile's largest weight, which
 //              divides O), writes P (bf16) back into TMEM over S, rescales O
 //              in TMEM when m grows by more than kRescaleThreshold (log2
-//              units), and writes its O row and lse in the epilogue.
-//   warp 8     TMA producer: Q tiles through a 3-buffer ring (so an item's
-//              Q_A can land while the previous item still runs), K/V copies
-//              in pairs {V_(j-1), K_j} through a 4-slot ring; an item's last
-//              V travels with the next item's K_0.
+//              units), and in the epilogue writes its lse and its O row into
+//              a shared-memory staging tile that one thread stores with TMA.
+//   warp 8     TMA producer: Q tiles through a 2-buffer ring (a tile's
+//              buffer takes the next item's tile once the tile's last S has
+//              been computed), K/V copies in pairs {V_(j-1), K_j} through a
+//              4-slot ring; an item's last V travels with the next item's K_0.
 //   warp 9     tcgen05 issuer (the whole warp runs the loop, one elected
 //              lane issues), also owns the TMEM allocation.
 //              Issue order per key tile j:
@@ -55,7 +56,7 @@ constexpr int kBN = 128;  // keys per tile
 constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
-constexpr int kQBuf = 3;  // Q buffers: the next item's Q_A loads while this item runs
+constexpr int kQBuf = 2;  // Q buffers: a tile's buffer takes the next item's tile once its last S is done
 constexpr int kRing = 4;  // K/V slots: K_j in slot 2j % 4, V_j in slot (2j+1) % 4
 // Copies travel in pairs: pair j = {V_(j-1), K_j} shares one completion
 // barrier and one release (pair slot j % 2): K_j and V_(j-1) are both done
@@ -70,6 +71,8 @@ template <int D>
 struct alignas(1024) PrefillSmem {
   uint8_t q[kQBuf][D / 64][kSubTileBytes];     // Q tiles, a ring over the CTA's tiles
   uint8_t ring[kRing][D / 64][kSubTileBytes];  // K/V tiles
+  uint8_t ostage[D / 64][kSubTileBytes];       // a finished O tile, bf16, as the O tensor map stores it
+  uint64_t stage_free;                    // the staged O tile has been read by its TMA store
   uint64_t q_full[kQBuf], q_free[kQBuf];  // Q tile landed / Q buffer no longer read
   uint64_t full[2], empty[2];  // per pair slot: pair j = {V_(j-1), K_j}
   uint64_t s_full[2], p_full[2], o_done[2], mma_fin;
@@ -202,7 +205,8 @@ __device__ __forceinline__ int item_index(int round) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const KernelParams p) {
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem<D>& sm = *reinterpret_cast<PrefillSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+    mbar_init(&sm.stage_free, 1);
     for (int b = 0; b < kQBuf; ++b) {
       mbar_init(&sm.q_full[b], 1);
       mbar_init(&sm.q_free[b], 1);
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   int issued_pairs[2] = {0, 0};    // producer: copy pairs issued per pair slot
-  int q_loads[kQBuf] = {0, 0, 0};  // producer: Q tiles issued per buffer
+  int q_loads[kQBuf] = {};  // producer: Q tiles issued per buffer
   bool mma_issued = false;
 
   if (warp == kWarpLoad) {
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv = smem_desc(smem_u32(&sm.ring[0][0][0]), kSubTileBytes, 1024, kSwizzle128B);
       int g = 0;                          // running pair index (as the producer's)
       int qt = 0;                         // running Q tile index (as the producer's)
-      int q_waits[kQBuf] = {0, 0, 0};     // completions of q_full[b] consumed
+      int q_waits[kQBuf] = {};            // completions of q_full[b] consumed
 
       // Pair g carries K_j and V_(j-1): K in ring slot (2g) % 4, V in slot
       // (2g + 3) % 4, i.e. slots 0 and 3 for even g, 2 and 1 for odd g.
@@ -436,12 +442,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_s = t_lane + tmem_s_col(x);
     const uint32_t t_o = t_lane + tmem_o_col(x);
     int s_waits = 0, o_waits = 0;
+    int e_base = 0;  // O tiles of this CTA's earlier items (the staging buffer's users, in order)
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int idx = item_index(round);
       if (idx >= p.n_items) break;
       const Item it = item_at(idx, p);
       const int row0 = it.m0 + x * kBM;
+      const int e_tile = e_base + x;  // tile A is staged before tile B
+      e_base += 1 + (it.m0 + kBM < p.Nq ? 1 : 0);
       if (row0 >= p.Nq) continue;  // this tile does not exist
       const int row = row0 + r;
       const int n_kv = it.ti[x].n_kv;
@@ -535,9 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
-      // O row -> 1/l_r -> bf16 -> straight to global memory (16-byte stores;
-      // rows past Nq are skipped), so the Q buffer is free for the next
-      // item as soon as its last S has been computed.
+      // O row -> 1/l_r -> bf16 -> the staging tile (128-byte swizzle, as
+      // the O tensor map stores it), then one thread stores the whole tile
+      // with TMA (rows past Nq are not written): the global writes are
+      // whole lines and the warps go on at once.  The staging tile is
+      // shared by the CTA's O tiles in item order, A before B.
       if (n_kv > 0) {
         if (!__all_sync(0xffffffffu, wait_or_abort(&sm.o_done[x], o_waits & 1, p, &sm.abort_flag))) break;
         ++o_waits;
@@ -549,7 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse = row_has_keys ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         p.lse[static_cast<size_t>(it.zq) * p.Nq + row] = lse;
       }
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(it.zq) * p.Nq + row) * D);
+      if (e_tile > 0 &&
+          !__all_sync(0xffffffffu, wait_or_abort(&sm.stage_free, (e_tile - 1) & 1, p, &sm.abort_flag)))
+        break;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -564,13 +577,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (row < p.Nq) {
+        // columns 32c .. 32c + 31: sub-tile c / 2, 16-byte chunks 4 (c % 2) ..
+        const uint32_t rb = smem_u32(&sm.ostage[c >> 1][0]) + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[c * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        }
+        for (int i = 0; i < 4; ++i)
+          st_shared_v4(rb + ((static_cast<uint32_t>((c & 1) * 4 + i) ^ static_cast<uint32_t>(r & 7)) << 4),
+                       w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
+      fence_proxy_async_smem();
       tc_fence_before_sync();
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + x) : "memory");  // this warpgroup's rows are staged
+      if (r == 0) {
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub) tma_store_3d(&tm_o, sm.ostage[sub], sub * 64, row0, it.zq);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&sm.stage_free);
+      }
     }
+    if (r == 0) bulk_wait_group0();  // this warpgroup's O stores have landed
   }
 
   // ------------------------------------------------------------ teardown
@@ -634,7 +659,7 @@ cudaError_t launch_d(const PrefillArgs& a, const DeviceGuard& g, cudaStream_t st
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (each holds all 512 TMEM columns)
   const int grid = static_cast<int>(min(n_items, static_cast<long long>(sms)));
-  prefill_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, kp);
+  prefill_kernel<D><<<grid, kThreads, smem, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, kp);
   return cudaGetLastError();
 }
 
