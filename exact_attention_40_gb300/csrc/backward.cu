@@ -28,6 +28,9 @@
 //     MN-major from shared memory.  With one query head per KV head it
 //     writes dK, dV directly; with GQA each query head writes fp32 partials
 //     that bwd_reduce_kernel sums in head order.
+// The dK/dV pass and the GQA sum are programmatic dependent launches: each
+// grid may start on SMs that the previous one has left while that one's
+// last CTAs finish, and waits for its results where it reads them.
 // Both passes are persistent (one CTA per SM, grid = min(units, SMs)); CTA
 // c takes unit r*G + c in even rounds r and r*G + G-1-c in odd ones, units
 // numbered heaviest first under the causal mask.  A CTA's TMA ring, product
@@ -160,6 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   BwdSmem<D, KV>& sm = *reinterpret_cast<BwdSmem<D, KV>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // The next launch of the backward (the dK/dV pass after the dQ pass, the
+  // GQA sum after the dK/dV pass) may be scheduled as soon as every CTA of
+  // this grid has started; it takes SMs as this grid's CTAs finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_units = p.n_tiles * p.n_bh;
@@ -343,6 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise warps
+    // dK/dV pass: D comes from the dQ pass, which may still be finishing
+    // when this grid starts (its copies and products need nothing from it).
+    if (KV) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int quarter = warp & 3;  // TMEM lanes 32 quarter ..
     const int half = warp >> 2;    // columns 32 half .. of the 64 streamed rows
     const int r = quarter * 32 + lane;
@@ -594,6 +604,7 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_reduce_kernel(const float* part, __nv_bfloat16* dk,
                                                          __nv_bfloat16* dv, long long n_elems, int G,
                                                          float scale) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the dK/dV pass's partials
   const long long i = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) * 4;
   if (i >= n_elems) return;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -659,12 +670,34 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     pk.n_tiles = (a.Nk + kStatRows - 1) / kStatRows;
     const long long units = static_cast<long long>(pk.n_tiles) * pk.n_bh;
     const long long grid = units < sms ? units : sms;
-    bwd_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem_kv, stream>>>(
-        *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64, *a.tm_k128, pk);
+    // programmatic dependent launches: each may start while the launch
+    // before it finishes, and waits for it where it reads its results
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_kv;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64,
+                           *a.tm_k128, pk);
+    if (e != cudaSuccess) return e;
     if (G > 1) {
       const long long n = static_cast<long long>(a.B) * a.Hkv * a.Nk * D;
-      bwd_reduce_kernel<D><<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
-          a.part, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), n, G, a.scale);
+      cudaLaunchConfig_t rc = {};
+      rc.gridDim = dim3(static_cast<unsigned>((n / 4 + 255) / 256));
+      rc.blockDim = dim3(256);
+      rc.dynamicSmemBytes = 0;
+      rc.stream = stream;
+      rc.attrs = pdl;
+      rc.numAttrs = 1;
+      const float* part = a.part;
+      e = cudaLaunchKernelEx(&rc, bwd_reduce_kernel<D>, part, static_cast<__nv_bfloat16*>(a.dk),
+                             static_cast<__nv_bfloat16*>(a.dv), n, G, a.scale);
+      if (e != cudaSuccess) return e;
     }
   }
   return cudaGetLastError();

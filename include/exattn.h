@@ -209,7 +209,9 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  * Two or three kernel launches on `stream`: dq (which also forms D) and
  * dk/dv on the tensor cores, each a persistent grid of at most one CTA per
  * SM; when query heads share a KV head, each writes fp32 partials to the
- * workspace and a third kernel sums them.  Asynchronous,
+ * workspace and a third kernel sums them.  The second and third are
+ * programmatic dependent launches (they may start as the previous launch
+ * drains).  Asynchronous,
  * deterministic (no atomics; sums in head order).  A bounded wait inside the
  * kernels that runs out sets EXATTN_DEVICE_TIMEOUT_BIT.
  */
