@@ -4,9 +4,12 @@ shape plus paged one-token decode, through the C ABI, on one GB300 per rank.
 One step = attn_fwd on the prefill workload, then attn_decode_paged on the
 decode workload (every row of the hot-path table runs once).  Inputs are
 seeded synthetic data (the generator in exact_attention_40_gb300.synth),
-resident in HBM before timing.  L2 is flushed (a 256 MiB write) before each
-step; the flush is outside the timed kernels.  Each kernel group is timed
-with CUDA events on the launching stream.
+resident in HBM before timing.  The step's inputs are larger than L2: the
+prefill takes six input sets (25.2 MB each) in turn and every decode sweeps
+1.18 GB of K/V, so no step finds its inputs in L2 and no flush runs between
+steps.  The same steps with a 256 MiB write flushing L2 before each (outside
+the timed kernels) are reported apart under "step_l2_flushed".  Each kernel
+group is timed with CUDA events on the launching stream.
 
 Prints one JSON line (rank 0).  `value` is prefill TFLOP/s (causal FLOPs
 4*B*Hq*Nq*Nk*d/2 over the summed prefill kernel time of the K timed steps,
@@ -299,21 +302,30 @@ def run_gpu(args):
     flush = torch.empty(256 * 1024 * 1024, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
+    # six prefill input sets, taken in turn by the steps (151 MB, more than L2)
+    import dataclasses
+    psets = [(q, k, v)]
+    for i in range(1, 6):
+        ci = dataclasses.replace(pc, seed=pc.seed + 1000 + i)
+        psets.append(tuple(to_dev(a) for a in synth.prefill_inputs(ci)))
+
     prefill_flops = pc.flops()
     decode_bytes = synth.decode_kv_bytes(dinp["ctx_lens"], dc.Hkv, dc.d)
     decode_bytes_all = decode_bytes + 2 * dinp["q"].nbytes + dinp["block_table"].nbytes + \
         dinp["ctx_lens"].nbytes + dc.num_seqs * dc.Hq * 4
 
-    def step(ev):
-        flush.fill_(1)
+    def step(ev, i, flushed=False):
+        if flushed:
+            flush.fill_(1)
+        qs, ks, vs = psets[i % len(psets)]
         ev[0].record(stream)
-        exattn.attn_fwd(q, k, v, causal=True, out=out, lse=lse)
+        exattn.attn_fwd(qs, ks, vs, causal=True, out=out, lse=lse)
         ev[1].record(stream)
         exattn.attn_decode_paged(dq, dk, dv, dbt, dcl, out=dout, lse=dlse, workspace=ws)
         ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    for i in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)], i)
     torch.cuda.synchronize()
     if exattn.attn_get_device_status() != 0:
         raise RuntimeError("device status word set during warm-up")
@@ -328,7 +340,7 @@ def run_gpu(args):
     t_wall = time.perf_counter()
     queue_ahead(torch)
     for i in range(args.steps):
-        step(events[i])
+        step(events[i], args.warmup + i)
     torch.cuda.synchronize()
     barrier(world)
     t_wall = time.perf_counter() - t_wall
@@ -347,6 +359,30 @@ def run_gpu(args):
     dec_avg_ms = dec_total / args.steps
     achieved = prefill_flops / (pre_avg_ms * 1e-3) / 1e12
     pre_spread, dec_spread = spread(pre_ms), spread(dec_ms)
+
+    # ---- the same steps with L2 flushed before each by a 256 MiB write: the
+    # flush leaves L2 full of dirty lines, whose write-back the following
+    # kernels pay for (the decode most: it evicts ~100 MB of them)
+    flushed = None
+    if args.flushed_steps > 0:
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.flushed_steps)]
+        torch.cuda.synchronize()
+        queue_ahead(torch)
+        for i in range(args.flushed_steps):
+            step(fev[i], i, flushed=True)
+        torch.cuda.synchronize()
+        if exattn.attn_get_device_status() != 0:
+            raise RuntimeError("device status word set by the flushed steps")
+        fp = spread([e[0].elapsed_time(e[1]) for e in fev])
+        fd = spread([e[1].elapsed_time(e[2]) for e in fev])
+        flushed = {"l2": "flushed before every step (256 MiB write, outside the timed kernels)",
+                   "steps": args.flushed_steps,
+                   "prefill_tflops": prefill_flops / (fp["ms_mean"] * 1e-3) / 1e12,
+                   "prefill_frac_bf16_peak": prefill_flops / (fp["ms_mean"] * 1e-3) / 1e12 / peaks["bf16"],
+                   "prefill_per_step": fp,
+                   "decode_gbs": decode_bytes / (fd["ms_mean"] * 1e-3) / 1e9,
+                   "decode_frac_hbm_peak": decode_bytes / (fd["ms_mean"] * 1e-3) / 1e9 / peaks["hbm"],
+                   "decode_per_step": fd}
 
     # ---- the decode step replayed from a captured CUDA graph (same kernels,
     # same buffers), L2 flushed before every replay, apart from the step
@@ -408,6 +444,33 @@ def run_gpu(args):
                 times[mode] = min(times.get(mode, 1e30), e0.elapsed_time(e1) / n_small)
         dgraph["small_8x512"] = {"us_direct": times["direct"] * 1e3, "us_graph": times["graph"] * 1e3,
                                  "steps_back_to_back": n_small}
+
+    # ---- the decode step back to back: 20 calls between one pair of events,
+    # no flush (each call reads 1.18 GB of K/V, far more than L2, so the
+    # next call finds little of it there); the per-call time then excludes
+    # what an event-bracketed launch pays outside the kernels' work
+    dec_b2b = None
+    if args.graph_steps > 0:
+        for _ in range(3):
+            exattn.attn_decode_paged(dq, dk, dv, dbt, dcl, out=dout, lse=dlse, workspace=ws)
+        runs = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            queue_ahead(torch)
+            e0.record(stream)
+            for _ in range(20):
+                exattn.attn_decode_paged(dq, dk, dv, dbt, dcl, out=dout, lse=dlse, workspace=ws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            runs.append(e0.elapsed_time(e1) / 20)
+        if exattn.attn_get_device_status() != 0:
+            raise RuntimeError("device status word set by the back-to-back decode")
+        ms_d = statistics.median(runs)
+        dec_b2b = {"us_per_call": ms_d * 1e3, "us_per_call_runs": [x * 1e3 for x in runs],
+                   "gbs": decode_bytes / (ms_d * 1e-3) / 1e9,
+                   "frac_hbm_peak": decode_bytes / (ms_d * 1e-3) / 1e9 / peaks["hbm"],
+                   "calls": 20, "l2": "inputs larger than L2, no flush"}
 
     # ---- attention backward on the prefill workload (dO ~ N(0,1)), timed
     # apart from the step; FLOPs = 2.5 x the forward's (the backward's five
@@ -493,12 +556,7 @@ def run_gpu(args):
         # around all of them.  The per-launch time then excludes what an
         # isolated, event-bracketed launch pays outside the kernel's work (an
         # empty 152-CTA kernel that allocates TMEM measures ~6 us that way).
-        import dataclasses
-        sets = []
-        for i in range(6):
-            ci = dataclasses.replace(pc, seed=pc.seed + 1000 + i)
-            sq_, sk_, sv_ = (to_dev(a) for a in synth.prefill_inputs(ci))
-            sets.append((sq_, sk_, sv_))
+        sets = psets
         bout = torch.empty_like(q)
         blse = torch.empty_like(lse)
         n_b2b = 12 * len(sets)
@@ -532,7 +590,7 @@ def run_gpu(args):
             frac_bf16_burst=prefill_flops / (ms_b * 1e-3) / 1e12 / peaks["bf16"],
             frac_bf16_sustained=prefill_flops / (ms_b * 1e-3) / 1e12 / peaks["bf16_sus"],
             l2="inputs larger than L2 (6 x 25.2 MB sets in turn), no flush", clocks=cl_)
-        del sets, bout, blse
+        del bout, blse
 
     # ---- end to end through the public API with pinned host buffers.  Every
     # step copies its q, k, v in from pinned host memory and reads its out
@@ -724,7 +782,8 @@ def run_gpu(args):
         "ms_per_step": (pre_total + dec_total) / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed before every step (256 MiB write, outside the timed kernels)",
+                   "l2": "no flush: the step's inputs are larger than L2 (six 25.2 MB prefill input "
+                         "sets taken in turn; each decode sweeps 1.18 GB of K/V)",
                    "wall_s_timed_region": t_wall},
         "prefill": {"tflops": achieved, "ms": pre_avg_ms, "per_step": pre_spread,
                     "tflops_median": prefill_flops / (pre_spread["ms_median"] * 1e-3) / 1e12,
@@ -752,6 +811,8 @@ def run_gpu(args):
         "add_rms_norm": norm,
         "rope_cache_write": rope,
         "decode_graph": dgraph,
+        "decode_back_to_back": dec_b2b,
+        "step_l2_flushed": flushed,
         "attn_bwd": bwd,
         "prefill_configs": configs,
         "gpu_launches": 3 * args.steps,
@@ -768,6 +829,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="exattn", choices=["exattn", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--flushed-steps", type=int, default=500,
+                    help="steps timed again with a 256 MiB L2 flush before each (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-calls", type=int, default=50,
                     help="attention backward calls on the prefill workload (0 skips it)")
