@@ -110,9 +110,10 @@ __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const B
   return bwd_wait_slow(bar, parity, p.wait_ns, p.status, ab);
 }
 
-// Which tiles a CTA works on.  KV: a 128-key block of one query head and the
+// The tiles of work unit u.  KV: a 128-key block of one query head and the
 // 64-row query tiles [first, first + count) that see any of its keys.  Q: a
-// 128-row query tile and the 64-key tiles [0, count) that it sees.
+// 128-row query tile and the 64-key tiles [0, count) that it sees.  Units
+// are numbered heaviest first under the causal mask.
 struct Work {
   int bh, tile;      // (b * Hq + hq), stationary tile index
   int splane, srow;  // stationary tensor plane and first row
@@ -120,14 +121,14 @@ struct Work {
 };
 
 template <bool KV>
-__device__ __forceinline__ Work work_of(int cta, const BwdParams& p) {
+__device__ __forceinline__ Work work_of(int u, const BwdParams& p) {
   Work w;
-  w.bh = cta % p.n_bh;
+  w.bh = u % p.n_bh;
   const int hq = w.bh % p.Hq, b = w.bh / p.Hq;
   const int kv_plane = b * p.Hkv + hq / (p.Hq / p.Hkv);
   const long long shift = static_cast<long long>(p.Nk) - p.Nq;
   if (KV) {
-    w.tile = cta / p.n_bh;  // key block; under the mask the first ones see the most queries
+    w.tile = u / p.n_bh;  // key block; under the mask the first ones see the most queries
     w.splane = kv_plane;
     w.srow = w.tile * kStatRows;
     w.rplane = w.bh;
@@ -140,7 +141,7 @@ __device__ __forceinline__ Work work_of(int cta, const BwdParams& p) {
     w.first = first;
     w.count = n_q - first;
   } else {
-    w.tile = p.n_tiles - 1 - cta / p.n_bh;  // query tile; the last ones see the most keys
+    w.tile = p.n_tiles - 1 - u / p.n_bh;  // query tile; the last ones see the most keys
     w.splane = w.bh;
     w.srow = w.tile * kStatRows;
     w.rplane = kv_plane;
@@ -184,8 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_r1);
     if (!KV) tma_prefetch_desc(&tm_o);
     mbar_init(&sm.stat_full, 1);
-    // released by the MMA warp's commit after a unit's last products and,
-    // in the dQ pass, by the eight elementwise warps once D is formed
+    // The stationary tiles are released by the MMA warp's commit after a
+    // unit's last products (dK/dV pass) or by the eight elementwise warps
+    // once they have formed D and copied Q and dO into TMEM (dQ pass); the
+    // TMEM copies are filled by those warps and released by the MMA warp's
+    // commit after the unit's last products.
     mbar_init(&sm.stat_free, KV ? 1 : 8);
     mbar_init(&sm.a_full, 8);
     mbar_init(&sm.a_free, 1);
