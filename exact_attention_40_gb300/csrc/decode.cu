@@ -23,6 +23,9 @@
 //   its partial output O_s (divided by the sum of the bf16 weights P V used)
 //   and lse_s (natural log, from the unrounded exponentials) to the
 //   workspace.
+//   When the block table cannot reach a second split (every sequence fits
+//   one), the split kernel writes the final output and log-sum-exp itself
+//   and the merge is not launched (it would weight the one split by 1).
 // decode_combine_kernel: one CTA per (sequence, query head):
 //   L = log sum_s exp(lse_s), o = sum_s exp(lse_s - L) O_s, lse = L.
 //   Launched with programmatic dependent launch so its launch overlaps the
@@ -64,6 +67,9 @@ struct SplitParams {
   const int32_t* ctx_lens;
   float* ws_o;
   float* ws_lse;
+  __nv_bfloat16* out;  // direct mode: the final output and log-sum-exp
+  float* lse;
+  int direct;          // every sequence fits one split: no partials, no merge
   unsigned int* status;
   unsigned long long wait_ns;
   int Hq, Hkv, group, n_chunks, num_blocks, max_blocks_per_seq, max_splits;
@@ -109,7 +115,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int max_ctx = p.max_blocks_per_seq * kBlk;
   const int ctx = clamp_ctx(__ldg(p.ctx_lens + seq), max_ctx, p.status);
   const int n_splits = (ctx + SPLIT - 1) / SPLIT;
-  if (split >= n_splits) return;  // whole CTA: nothing of this sequence here
+  if (split >= n_splits) {  // whole CTA: nothing of this sequence here
+    if (p.direct && n_splits == 0 && split == 0) {
+      // direct mode, no cached token: o = 0, lse = -inf for this CTA's heads
+      const int h0 = hkv * p.group + chunk * kRows;
+      const int rows = min(kRows, p.group - chunk * kRows);
+      for (int idx = threadIdx.x; idx < rows * D; idx += kThreads) {
+        const size_t row = static_cast<size_t>(seq) * p.Hq + h0 + idx / D;
+        p.out[row * D + idx % D] = __float2bfloat16_rn(0.f);
+        if (p.lse != nullptr && idx % D == 0) p.lse[row] = -INFINITY;
+      }
+    }
+    return;
+  }
 
   const int tok0 = split * SPLIT;
   const int tok_end = min(ctx, tok0 + SPLIT);
@@ -329,8 +347,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     const size_t slot = (static_cast<size_t>(seq) * p.Hq + hq0 + r) * p.max_splits + split;
     // the split's output divides by the sum of the weights P V used; its
     // log-sum-exp keeps the sum of the unrounded exponentials
-    p.ws_o[slot * D + col] = (L > 0.f) ? o / Lr : 0.f;
-    if (col == 0) p.ws_lse[slot] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    const float os = (L > 0.f) ? o / Lr : 0.f;
+    const float ls = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    if (p.direct) {
+      // the only split: the merge would weight it by exactly 1
+      const size_t row = static_cast<size_t>(seq) * p.Hq + hq0 + r;
+      p.out[row * D + col] = __float2bfloat16_rn(os);
+      if (p.lse != nullptr && col == 0) p.lse[row] = ls;
+    } else {
+      p.ws_o[slot * D + col] = os;
+      if (col == 0) p.ws_lse[slot] = ls;
+    }
   }
 }
 
@@ -387,6 +414,11 @@ cudaError_t launch_ds(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t st
   sp.ctx_lens = a.ctx_lens;
   sp.ws_o = a.ws_o;
   sp.ws_lse = a.ws_lse;
+  sp.out = static_cast<__nv_bfloat16*>(a.out);
+  sp.lse = a.lse;
+  // Block tables too short to reach a second split: each sequence has at
+  // most one, so the split kernel writes the result and no merge runs.
+  sp.direct = static_cast<long long>(a.max_blocks_per_seq) * kBlk <= SPLIT ? 1 : 0;
   sp.status = g.status;
   sp.wait_ns = g.wait_ns;
   sp.Hq = a.Hq;
@@ -405,7 +437,7 @@ cudaError_t launch_ds(const DecodeArgs& a, const DeviceGuard& g, cudaStream_t st
   dim3 grid((a.max_blocks_per_seq * kBlk + SPLIT - 1) / SPLIT, a.Hkv * sp.n_chunks, a.num_seqs);
   decode_split_kernel<D, SPLIT><<<grid, kThreads, smem, stream>>>(*a.tm_k, *a.tm_v, sp);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || sp.direct) return e;
 
   CombineParams cp;
   cp.ws_o = a.ws_o;

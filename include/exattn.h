@@ -109,7 +109,9 @@ size_t attn_decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_p
  * byte); each split yields a partial output and log-sum-exp, and a second
  * kernel merges them (exact up to rounding).  The workspace is sized for
  * 512-token splits either way.
- * Two kernel launches.  num_blocks >= 1.  A ctx_len of 0 gives o = 0, lse = -inf; a
+ * Two kernel launches; one when max_blocks_per_seq * block_size <= 512 (no
+ * sequence can have a second split, so the split kernel writes the result
+ * and no merge runs; same bits).  num_blocks >= 1.  A ctx_len of 0 gives o = 0, lse = -inf; a
  * ctx_len above max_blocks_per_seq * block_size or a table entry outside
  * [0, num_blocks) is clamped/skipped and flagged in the device status word.
  */

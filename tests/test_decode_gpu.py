@@ -112,3 +112,18 @@ def test_no_lse_and_workspace_reuse(env):
     assert got_l is None
     ref_o, ref_l = oracle(env, inp, 0.1)
     assert_parity(metrics(got_o, None, ref_o, ref_l), "no lse")
+
+
+def test_single_split_tables_write_directly(env):
+    """Block tables that cannot reach a second 512-token split: the split
+    kernel writes the result itself (no merge launch).  Same bits as the
+    merged path, which a wider table (spare columns) forces."""
+    inp = synth.decode_inputs_lens(68, np.array([0, 200, 512, 1, 77], np.int32), 8, 2, 128)
+    assert inp["block_table"].shape[1] * 16 <= 512
+    got_o, got_l = run(env, inp, 0.1)
+    ref_o, ref_l = oracle(env, inp, 0.1)
+    assert np.all(got_o[0] == 0) and np.all(got_l[0] == -np.inf)
+    assert_parity(metrics(got_o, got_l, ref_o, ref_l), "single split")
+    wide = np.concatenate([inp["block_table"], np.full((5, 8), -1, np.int32)], axis=1)
+    w_o, w_l = run(env, dict(inp, block_table=wide), 0.1)
+    assert np.array_equal(got_o, w_o) and np.array_equal(got_l, w_l)
