@@ -13,6 +13,7 @@ callers (and tests) that pass pointers themselves.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -98,6 +99,15 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _on_device(t):
+    """Context that makes t's device current for the call; a no-op (no device
+    switch and restore) when it already is, as in a single-GPU loop."""
+    import torch
+    if t.device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(t.device)
+
+
 def _check_tensor(name, t, dtype, ndim):
     import torch
     if not isinstance(t, torch.Tensor):
@@ -135,7 +145,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
         lse = torch.empty((B, Hq, Nq), device=q.device, dtype=torch.float32)
     elif lse is not None:
         _check_tensor("lse", lse, torch.float32, 3)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                           lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Nq, Nk, d,
                           float(scale), int(bool(causal)), _stream_handle(stream))
@@ -168,10 +178,10 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, ctx_lens, scale: float |
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((S, Hq), device=q.device, dtype=torch.float32)
-    need = attn_decode_workspace_bytes(S, Hq, d, max_blocks, bs)
-    if workspace is None:
+    if workspace is None:  # (the library checks a given workspace's size)
+        need = attn_decode_workspace_bytes(S, Hq, d, max_blocks, bs)
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib.attn_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                    block_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
                                    lse.data_ptr() if lse is not None else None, S, Hq, Hkv, d, bs,
@@ -207,7 +217,7 @@ def attn_add_rms_norm(x, residual, weight, eps: float = 1e-6, out=None, residual
         _check_tensor("residual_out", residual_out, torch.bfloat16, 2)
     if tuple(out.shape) != (T, D) or tuple(residual_out.shape) != (T, D):
         raise ValueError("output shape mismatch")
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         rc = lib.attn_add_rms_norm(x.data_ptr(), residual.data_ptr(), weight.data_ptr(),
                                    out.data_ptr(), residual_out.data_ptr(), T, D, float(eps),
                                    _stream_handle(stream))
@@ -238,7 +248,7 @@ def attn_rope_cache_write(q, k, v, seq_ids, positions, block_table, k_cache, v_c
             or positions.shape[0] != T:
         raise ValueError("shape mismatch")
     S, max_blocks = block_table.shape
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib.attn_rope_cache_write(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_ids.data_ptr(),
                                        positions.data_ptr(), block_table.data_ptr(),
                                        k_cache.data_ptr(), v_cache.data_ptr(), T, Hq, Hkv, d, S,
@@ -306,7 +316,7 @@ def attn_decode_graph_capture(q, k_cache, v_cache, block_table, ctx_lens, scale:
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     h = ctypes.c_void_p()
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib.attn_decode_graph_capture(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                            block_table.data_ptr(), ctx_lens.data_ptr(), out.data_ptr(),
                                            lse.data_ptr() if lse is not None else None, S, Hq, Hkv, d,
@@ -341,7 +351,7 @@ def attn_bwd(q, k, v, out, dout, lse, causal: bool = False, scale: float | None 
     need = int(lib.attn_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d))
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Nq,
                           Nk, d, float(scale), int(bool(causal)), workspace.data_ptr(),
