@@ -14,7 +14,7 @@
 // next item's Q copy and first S = Q K^T overlap the previous item's
 // epilogue, whose O tile leaves through one TMA store.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3  softmax warpgroup of tile A; warps 4-7 that of tile B.  Thread
 //              r of a warpgroup owns query row r of its tile, which is TMEM
 //              lane r.  It reads S from TMEM, masks, keeps the running max m
@@ -23,13 +23,16 @@
 //              divides O), writes P (bf16) back into TMEM over S, rescales O
 //              in TMEM when m grows by more than kRescaleThreshold (log2
 //              units), and in the epilogue writes its lse and its O row into
-//              a shared-memory staging tile that one thread stores with TMA.
+//              a shared-memory staging tile.
 //   warp 8     TMA producer: Q tiles through a 2-buffer ring (a tile's
 //              buffer takes the next item's tile once the tile's last S has
 //              been computed), K/V copies in pairs {V_(j-1), K_j} through a
 //              4-slot ring; an item's last V travels with the next item's K_0.
 //   warp 9     tcgen05 issuer (the whole warp runs the loop, one elected
 //              lane issues), also owns the TMEM allocation.
+//   warp 10    issues each staged O tile's TMA store and releases the
+//              staging tile once the copy has read it, so no softmax warp
+//              waits for a store.
 //              Issue order per key tile j:
 //                S_A = Q_A K_j^T,  O_B += P_B(j-1) V_(j-1),  S_B = Q_B K_j^T,
 //                O_A += P_A(j) V_j
@@ -53,9 +56,10 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;  // keys per tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpStore = 10;  // issues the O tiles' TMA stores
 constexpr int kQBuf = 2;  // Q buffers: a tile's buffer takes the next item's tile once its last S is done
 constexpr int kRing = 4;  // K/V slots: K_j in slot 2j % 4, V_j in slot (2j+1) % 4
 // Copies travel in pairs: pair j = {V_(j-1), K_j} shares one completion
@@ -73,6 +77,7 @@ struct alignas(1024) PrefillSmem {
   uint8_t ring[kRing][D / 64][kSubTileBytes];  // K/V tiles
   uint8_t ostage[D / 64][kSubTileBytes];       // a finished O tile, bf16, as the O tensor map stores it
   uint64_t stage_free;                    // the staged O tile has been read by its TMA store
+  uint64_t staged;                        // the four warps of a tile's warpgroup have staged their rows
   uint64_t q_full[kQBuf], q_free[kQBuf];  // Q tile landed / Q buffer no longer read
   uint64_t full[2], empty[2];  // per pair slot: pair j = {V_(j-1), K_j}
   uint64_t s_full[2], p_full[2], o_done[2], mma_fin;
@@ -220,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
     mbar_init(&sm.stage_free, 1);
+    mbar_init(&sm.staged, 4);
     for (int b = 0; b < kQBuf; ++b) {
       mbar_init(&sm.q_full[b], 1);
       mbar_init(&sm.q_free[b], 1);
@@ -434,6 +440,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         g = base + n_iter;
       }
     }
+  } else if (warp == kWarpStore) {
+    // ------------------------------------------------------------ O stores
+    // The CTA's O tiles in the softmax warpgroups' order (per item, A then
+    // B, tiles that exist): once a tile is staged, one TMA store of it, and
+    // the staging tile is released as soon as the copy has read it.
+    if (lane == 0) {
+      int e = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int idx = item_index(round);
+        if (idx >= p.n_items) break;
+        const Item it = item_at(idx, p);
+        for (int x = 0; x < 2 && ok; ++x) {
+          const int row0 = it.m0 + x * kBM;
+          if (row0 >= p.Nq) continue;
+          if (!(ok = wait_or_abort(&sm.staged, e & 1, p, &sm.abort_flag))) break;
+#pragma unroll
+          for (int sub = 0; sub < D / 64; ++sub) tma_store_3d(&tm_o, sm.ostage[sub], sub * 64, row0, it.zq);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&sm.stage_free);
+          ++e;
+        }
+      }
+      bulk_wait_group0();  // the O stores have landed
+    }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int x = warp >> 2;                 // 0: tile A, 1: tile B
@@ -586,16 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
-      asm volatile("bar.sync %0, 128;" ::"r"(1 + x) : "memory");  // this warpgroup's rows are staged
-      if (r == 0) {
-#pragma unroll
-        for (int sub = 0; sub < D / 64; ++sub) tma_store_3d(&tm_o, sm.ostage[sub], sub * 64, row0, it.zq);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(&sm.stage_free);
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.staged);  // this warp's rows are staged: the store warp takes it
     }
-    if (r == 0) bulk_wait_group0();  // this warpgroup's O stores have landed
   }
 
   // ------------------------------------------------------------ teardown
