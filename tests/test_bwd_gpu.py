@@ -5,10 +5,11 @@ against the fp64 oracle, which computes them from Q, K, V and dO alone.
 Bar, derived from the arithmetic: the products run on bf16 operands with
 fp32 accumulation; P and dS are rounded to bf16 (relative 2^-9) before the
 dV, dK and dQ products, D comes from the bf16 forward output, and each
-result is rounded to bf16 once.  The relative errors of the terms are a few
-times 2^-9 and mostly average out, so each gradient must satisfy
-rel-RMS = ||g - ref|| / ||ref|| <= 1e-2 and max |g - ref| <= 5e-2 max |ref|
-+ 1e-4.  The absolute 1e-4 covers entries whose exact value is 0 while the
+result is rounded to bf16 once.  Each rounding contributes about 2^-9
+(2e-3) relative, independently per term, so the sums' relative RMS error
+stays near 2^-9 and the forward's bar applies: each gradient must satisfy
+rel-RMS = ||g - ref|| / ||ref|| <= 5e-3 and max |g - ref| <= 2e-2 max |ref|
++ 1e-4 (about ten rounding units at the largest entry).  The absolute 1e-4 covers entries whose exact value is 0 while the
 kernel's is not: with D taken from the bf16 O, dP - D keeps a residue of
 about 2^-9 |dO| |v| where it is exactly zero (a row with one visible key)."""
 import numpy as np
@@ -19,8 +20,8 @@ from helpers import to_dev
 
 pytestmark = pytest.mark.gpu
 
-REL_RMS = 1e-2
-MAX_REL = 5e-2
+REL_RMS = 5e-3
+MAX_REL = 2e-2
 MAX_ABS = 1e-4
 
 
