@@ -529,7 +529,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   if (need > 0 && !aligned16(workspace)) return EXATTN_ERR_ALIGNMENT;
   exattn::BwdArgs a;
   exattn::DeviceGuard g;
-  CUtensorMap maps[9];  // copied into the launches' parameters
+  CUtensorMap maps[10];  // copied into the launches' parameters
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
@@ -542,6 +542,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
       if ((rc = tensor_map(dev, q, d, Nq, pq, &maps[4], 128)) != EXATTN_OK) return rc;
       if ((rc = tensor_map(dev, dout, d, Nq, pq, &maps[5], 128)) != EXATTN_OK) return rc;
       if ((rc = tensor_map(dev, out, d, Nq, pq, &maps[8], 128)) != EXATTN_OK) return rc;
+      if ((rc = tensor_map(dev, dq, d, Nq, pq, &maps[9], 128)) != EXATTN_OK) return rc;
     }
     if (Nk > 0) {
       if ((rc = tensor_map(dev, k, d, Nk, pk, &maps[2], 128)) != EXATTN_OK) return rc;
@@ -550,7 +551,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
       if ((rc = tensor_map(dev, v, d, Nk, pk, &maps[7], 64)) != EXATTN_OK) return rc;
     }
     // an empty side has no tiles to load: its maps are stand-ins, never used
-    if (Nq == 0) maps[0] = maps[1] = maps[4] = maps[5] = maps[8] = maps[2];
+    if (Nq == 0) maps[0] = maps[1] = maps[4] = maps[5] = maps[8] = maps[9] = maps[2];
     if (Nk == 0) maps[2] = maps[3] = maps[6] = maps[7] = maps[0];
   }
   g.wait_ns = wait_budget_ns();
@@ -563,6 +564,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   a.tm_k64 = &maps[6];
   a.tm_v64 = &maps[7];
   a.tm_o128 = &maps[8];
+  a.tm_dq128 = &maps[9];
   a.q = q;
   a.k = k;
   a.v = v;

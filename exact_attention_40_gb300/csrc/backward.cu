@@ -10,12 +10,14 @@
 // stored.  Kernels (no atomics, deterministic), in launch order:
 //   * bwd_tc_kernel<D, false> (dQ pass): a unit is a 128-row query tile of
 //     one head.  Its Q, dO and O tiles come into shared memory; the
-//     elementwise warps form D for their rows from dO and O (written for the
-//     dK/dV pass) and copy the Q and dO rows into TMEM, where they are the A
-//     operands of S = Q K^T and dP = dO V^T (M128 N64, B = the streamed
-//     64-key K and V tiles of a 4-stage TMA ring), so the tensor core reads
-//     only the streamed tiles from shared memory.  dS = P (dP - D) goes back
-//     to TMEM as bf16 and dQ += dS K accumulates in TMEM;
+//     elementwise warps form D for their rows from dO and O (each half of
+//     the warps over its half of the columns; written for the dK/dV pass)
+//     and copy the Q and dO rows into TMEM, where they are the A operands of
+//     S = Q K^T and dP = dO V^T (M128 N64, B = the streamed 64-key K and V
+//     tiles of a 4-stage TMA ring), so the tensor core reads only the
+//     streamed tiles from shared memory.  dS = P (dP - D) goes back to TMEM
+//     as bf16 and dQ += dS K accumulates in TMEM.  dQ leaves through the O
+//     tile's slot: staged there in bf16 and written by a TMA store;
 //   * bwd_tc_kernel<D, true> (dK/dV pass): a unit is a 128-key block of one
 //     query head.  K and V stay in shared memory; the 64-row query tiles of
 //     that head that the mask leaves stream through the ring.  Per tile the
@@ -37,9 +39,9 @@
 // buffers and accumulators run on across its units: the next unit's
 // stationary tiles load while the current one drains, and its first
 // products are queued before the previous unit's epilogue is done.
-// Warp roles (320 threads): warps 0-7 elementwise, warp 8 TMA producer,
+// Warp roles (352 threads): warps 0-7 elementwise, warp 8 TMA producer,
 // warp 9 tcgen05 issuer (warp-uniform loop, one elected lane issues) and
-// owner of the TMEM allocation.  Every wait is bounded; a wait that runs
+// owner of the TMEM allocation, warp 10 the dQ pass's TMA stores.  Every wait is bounded; a wait that runs
 // out sets the device status word, drains what is in flight, frees TMEM and
 // returns.
 #include <cuda_bf16.h>
@@ -50,9 +52,10 @@
 namespace exattn {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpStore = 10;  // dQ pass: TMA stores of dQ
 constexpr int kStatRows = 128;   // rows of a stationary tile (= TMEM lanes)
 constexpr int kStreamRows = 64;  // rows of a streamed tile (= columns of S, dP)
 constexpr int kStages = 4;
@@ -70,8 +73,11 @@ struct alignas(1024) BwdSmem {
   uint8_t stat[2][D / 64][kStatSub];              // K, V (dK/dV pass) or Q, dO (dQ pass)
   uint8_t ring[kStages][2][D / 64][kStreamSub];   // Q, dO (dK/dV pass) or K, V (dQ pass)
   uint8_t otile[KV ? 1 : D / 64][KV ? 16 : kStatSub];  // dQ pass: O, for D = rowsum(dO * O)
+  float dpart[KV ? 1 : 2][KV ? 1 : kStatRows];          // dQ pass: D of each half of the columns
   uint64_t stat_full, stat_free, full[kStages], empty[kStages], s_full[2], p_full[2], acc_done, acc_free, fin;
   uint64_t a_full, a_free;  // dQ pass: Q and dO rows in TMEM
+  uint64_t dpart_full;      // dQ pass: both halves' shares of D written
+  uint64_t dq_staged;       // dQ pass: the tiles read (first phase), then each unit's dQ staged
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -120,6 +126,16 @@ struct Work {
   int rplane, first, count;
 };
 
+// a = b = +0 unless lo <= c < hi (one predicate, two selects)
+__device__ __forceinline__ void keep_in_range(int c, int lo, int hi, uint32_t& a, uint32_t& b) {
+  asm("{\n\t.reg .pred q;\n\t"
+      "setp.ge.s32 q, %2, %3;\n\t"
+      "setp.lt.and.s32 q, %2, %4, q;\n\t"
+      "selp.b32 %0, %0, 0, q;\n\t"
+      "selp.b32 %1, %1, 0, q;\n\t}"
+      : "+r"(a), "+r"(b) : "r"(c), "r"(lo), "r"(hi));
+}
+
 template <bool KV>
 __device__ __forceinline__ Work work_of(int u, const BwdParams& p) {
   Work w;
@@ -160,7 +176,8 @@ template <int D, bool KV>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1,
                   const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
-                  const __grid_constant__ CUtensorMap tm_o, const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dq,
+                  const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   BwdSmem<D, KV>& sm = *reinterpret_cast<BwdSmem<D, KV>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -183,16 +200,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_s1);
     tma_prefetch_desc(&tm_r0);
     tma_prefetch_desc(&tm_r1);
-    if (!KV) tma_prefetch_desc(&tm_o);
+    if (!KV) {
+      tma_prefetch_desc(&tm_o);
+      tma_prefetch_desc(&tm_dq);
+    }
     mbar_init(&sm.stat_full, 1);
     // The stationary tiles are released by the MMA warp's commit after a
-    // unit's last products (dK/dV pass) or by the eight elementwise warps
-    // once they have formed D and copied Q and dO into TMEM (dQ pass); the
-    // TMEM copies are filled by those warps and released by the MMA warp's
-    // commit after the unit's last products.
-    mbar_init(&sm.stat_free, KV ? 1 : 8);
+    // unit's last products (dK/dV pass) or by the store warp (dQ pass): the
+    // O tile's slot then stages the previous unit's dQ, written by each
+    // elementwise warp over the bytes of O that it has read, and is free
+    // once the TMA store has read it.  The TMEM copies of Q and dO are
+    // filled by the elementwise warps and released by the MMA warp's commit
+    // after the unit's last products.
+    mbar_init(&sm.stat_free, 1);
     mbar_init(&sm.a_full, 8);
     mbar_init(&sm.a_free, 1);
+    mbar_init(&sm.dpart_full, 8);
+    mbar_init(&sm.dq_staged, 8);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
@@ -352,6 +376,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tiles += n;
       ++units;
     }
+  } else if (warp == kWarpStore) {
+    // ------------------------------------------------------------ dQ stores
+    // dQ pass: phase 0 of dq_staged = every warp has read the first unit's
+    // tiles; phase k > 0 = the dQ of the CTA's unit k - 1 is staged.  After
+    // each, the stationary tiles may be reloaded: for k > 0 once the TMA
+    // store of that dQ has read the staging tile.
+    if (!KV && lane == 0) {
+      bool ok = bwd_wait(&sm.dq_staged, 0, p, &sm.abort_flag);
+      if (ok) mbar_arrive(&sm.stat_free);
+      for (int round = 0; ok; ++round) {
+        const int u = unit_of(round);
+        if (u >= n_units) break;
+        if (!(ok = bwd_wait(&sm.dq_staged, (round + 1) & 1, p, &sm.abort_flag))) break;
+        const Work w = work_of<KV>(u, p);
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub) tma_store_3d(&tm_dq, sm.otile[sub], sub * 64, w.srow, w.bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&sm.stat_free);
+      }
+      bulk_wait_group0();  // the dQ stores have landed
+    }
   } else {
     // ------------------------------------------------------------ elementwise warps
     // dK/dV pass: D comes from the dQ pass, which may still be finishing
@@ -364,34 +410,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long shift = static_cast<long long>(p.Nk) - p.Nq;
     bool ok = true;
     int units = 0, tiles = 0, acc_units = 0;
-    // dQ pass, once per unit and before the previous unit's epilogue: D of
-    // this thread's query row from the dO and O tiles (rows past Nq read as
-    // zero), written by the first half for the dK/dV pass; then this half's
-    // share of the Q and dO row into the TMEM A operands, once the previous
-    // unit's products have read them.  The shared-memory tiles are released
-    // as soon as they are read, so the next unit's can load meanwhile.
-    float nxt_lse2 = 0.f, nxt_d = 0.f;
-    auto prologue = [&](int rnd, float& lse2_out, float& d_out) -> bool {
+    // dQ pass, once per unit and before the previous unit's epilogue: each
+    // half of the warps reads its half of the columns of this thread's dO, O
+    // and Q rows (rows past Nq read as zero) and forms its share of D; the
+    // tiles are released as soon as they are read, so the next unit's can
+    // load meanwhile.  Once the previous unit's products have read them, the
+    // Q and dO halves go into the TMEM A operands; the two shares of D meet
+    // in shared memory (first half + second half, the same sum in both) and
+    // the first half writes D for the dK/dV pass.
+    float nxt_lse = 0.f, nxt_d = 0.f;
+    auto prologue = [&](int rnd, float& lse_out, float& d_out) -> bool {
       const Work wq = work_of<KV>(unit_of(rnd), p);
       const int qrow = wq.srow + r;
       const size_t l0 = static_cast<size_t>(wq.bh) * p.Nq;
-      lse2_out = qrow < p.Nq ? p.lse[l0 + qrow] * kLog2e : 0.f;
+      lse_out = qrow < p.Nq ? p.lse[l0 + qrow] : 0.f;  // natural log; scaled where it is used
       if (!__all_sync(0xffffffffu, bwd_wait(&sm.stat_full, rnd & 1, p, &sm.abort_flag))) return false;
       const uint8_t* qb = &sm.stat[0][0][0];
       const uint8_t* dob = &sm.stat[1][0][0];
       const uint8_t* ob = &sm.otile[0][0];
       float acc = 0.f;
-#pragma unroll
-      for (int sub = 0; sub < D / 64; ++sub)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t off = sub * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-          float fo[8], fd[8];
-          unpack_bf16x8(*reinterpret_cast<const uint4*>(ob + off), fo);
-          unpack_bf16x8(*reinterpret_cast<const uint4*>(dob + off), fd);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc = fmaf(fd[e], fo[e], acc);
-        }
       uint32_t qv[D / 4], dv[D / 4];  // elements [half * D / 2, + D / 2) of the row, two a word
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
@@ -399,14 +436,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t off = (cc >> 3) * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + (((cc & 7) ^ (r & 7)) << 4);
         const uint4 a = *reinterpret_cast<const uint4*>(qb + off);
         const uint4 b = *reinterpret_cast<const uint4*>(dob + off);
+        float fo[8], fd[8];
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(ob + off), fo);
+        unpack_bf16x8(b, fd);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(fd[e], fo[e], acc);
         qv[4 * c] = a.x; qv[4 * c + 1] = a.y; qv[4 * c + 2] = a.z; qv[4 * c + 3] = a.w;
         dv[4 * c] = b.x; dv[4 * c + 1] = b.y; dv[4 * c + 2] = b.z; dv[4 * c + 3] = b.w;
       }
-      d_out = acc;
-      if (half == 0 && qrow < p.Nq) p.dsum[l0 + qrow] = acc;
+      // The first unit's tiles are free once read; a later unit's once the
+      // previous unit's dQ, staged after this read, has been stored.
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.stat_free);  // the Q, dO and O tiles may be reloaded
+      if (rnd == 0 && lane == 0) mbar_arrive(&sm.dq_staged);
+      // After a_free (which follows a_full) every warp has read the previous
+      // unit's shares of D.
       if (rnd > 0 && !__all_sync(0xffffffffu, bwd_wait(&sm.a_free, (rnd - 1) & 1, p, &sm.abort_flag))) return false;
+      sm.dpart[half][r] = acc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.dpart_full);
       tc_fence_after_sync();
       const uint32_t qc = t_lane + kQCol + static_cast<uint32_t>(half * (D / 4));
       if constexpr (D == 128) {
@@ -417,9 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_32x32b_x16(qc + D / 2, *reinterpret_cast<const uint32_t(*)[16]>(&dv[0]));
       }
       tmem_st_wait();
+      // Both shares are read before a_full: the next unit's shares are
+      // written only after a_free, which follows a_full.
+      if (!__all_sync(0xffffffffu, bwd_wait(&sm.dpart_full, rnd & 1, p, &sm.abort_flag))) return false;
+      const float dd = sm.dpart[0][r] + sm.dpart[1][r];
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.a_full);
+      d_out = dd;
+      if (half == 0 && qrow < p.Nq) p.dsum[l0 + qrow] = dd;
       return true;
     };
     for (int round = 0; ok; ++round) {
@@ -431,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t lrow0 = static_cast<size_t>(w.bh) * p.Nq;
       float row_lse2 = 0.f, row_d = 0.f;
       if constexpr (!KV) {
-        if (round == 0 && !(ok = prologue(0, nxt_lse2, nxt_d))) break;
-        row_lse2 = nxt_lse2;
+        if (round == 0 && !(ok = prologue(0, nxt_lse, nxt_d))) break;
+        row_lse2 = nxt_lse * kLog2e;
         row_d = nxt_d;
       }
       for (int i = 0; i < n; ++i) {
@@ -444,26 +497,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           col_lse2 = p.lse[lrow0 + c0 + lane] * kLog2e;
           col_d = p.dsum[lrow0 + c0 + lane];
         }
+        // This warp's 32 x 32 block: rows r_lo.. (keys in the dK/dV pass,
+        // queries in the dQ pass), streamed columns c_lo..
+        const long long r_lo = w.srow + quarter * 32, r_hi = r_lo + 31;
+        const long long c_lo = c0, c_hi = c0 + 31;
+        // every element visible and in range: no mask test
+        const bool interior = KV ? (r_hi < p.Nk && c_hi < p.Nq && (!p.causal || r_hi <= c_lo + shift))
+                                 : (r_hi < p.Nq && c_hi < p.Nk && (!p.causal || c_hi <= r_lo + shift));
+        // no element visible: P and dS are zero, the products are not read
+        const bool hidden = KV ? (r_lo >= p.Nk || c_lo >= p.Nq || (p.causal && r_lo > c_hi + shift))
+                               : (r_lo >= p.Nq || c_lo >= p.Nk || (p.causal && c_lo > r_hi + shift));
         if (!__all_sync(0xffffffffu, bwd_wait(&sm.s_full[b], (t >> 1) & 1, p, &sm.abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t col = kBufCol + 128u * b + half * 32;
-        uint32_t sv[32], dpv[32];
-        tmem_ld_32x32b_x32(t_lane + col, sv);
-        tmem_ld_32x32b_x32(t_lane + col + 64, dpv);
-        tmem_ld_wait();
         uint32_t pk[16], dsk[16];
-        // Is every element of this warp's 32 x 32 block visible and in range?
-        // Then no element needs a mask test.
-        const long long r_lo = w.srow + quarter * 32, r_hi = r_lo + 31;  // this warp's rows
-        const long long c_lo = c0, c_hi = c0 + 31;                       // this warp's columns
-        const bool interior = KV ? (r_hi < p.Nk && c_hi < p.Nq && (!p.causal || r_hi <= c_lo + shift))
-                                 : (r_hi < p.Nq && c_hi < p.Nk && (!p.causal || c_hi <= r_lo + shift));
-        if (interior) {
+        if (hidden) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = dsk[c] = 0u;
+        } else {
+          uint32_t sv[32], dpv[32];
+          tmem_ld_32x32b_x32(t_lane + col, sv);
+          tmem_ld_32x32b_x32(t_lane + col + 64, dpv);
+          tmem_ld_wait();
+          // Visible columns of this thread's row: c in [lo, hi).  dQ pass
+          // (row = query): keys below Nk and, causal, at most row + shift.
+          // dK/dV pass (row = key): queries below Nq and, causal, at least
+          // row - shift.  A row past the end sees nothing.
+          int lo = 0, hi = 32;
+          if (!interior) {
+            long long l = 0, h;
+            if (KV) {
+              h = row < p.Nk ? static_cast<long long>(p.Nq) - c0 : 0;
+              if (p.causal) l = static_cast<long long>(row) - shift - c0;
+            } else {
+              h = row < p.Nq ? static_cast<long long>(p.Nk) - c0 : 0;
+              if (p.causal) h = min(h, static_cast<long long>(row) + shift - c0 + 1);
+            }
+            lo = static_cast<int>(max(0ll, min(l, 32ll)));
+            hi = static_cast<int>(max(0ll, min(h, 32ll)));
+          }
           const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const float l2a = KV ? __shfl_sync(0xffffffffu, col_lse2, c) : row_lse2;
             const float l2b = KV ? __shfl_sync(0xffffffffu, col_lse2, c + 1) : row_lse2;
@@ -472,32 +549,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, f2_pack(-l2a, -l2b));
             float x0, x1;
             f2_unpack(x2, x0, x1);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            uint32_t p0 = __float_as_uint(ex2_approx(x0)), p1 = __float_as_uint(ex2_approx(x1));
             const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), f2_pack(-da, -db));
-            float d0, d1;
-            f2_unpack(f2_mul(f2_pack(p0, p1), t2), d0, d1);
-            pk[c / 2] = pack_bf16x2(p0, p1);
-            dsk[c / 2] = pack_bf16x2(d0, d1);
-          }
-        } else {
-  #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float pr[2], ds[2];
-  #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int cc = c + e;
-              // (key, query) of this element
-              const long long key = KV ? row : c0 + cc;
-              const long long qry = KV ? c0 + cc : row;
-              const float l2 = KV ? __shfl_sync(0xffffffffu, col_lse2, cc) : row_lse2;
-              const float dd = KV ? __shfl_sync(0xffffffffu, col_d, cc) : row_d;
-              const bool vis = key < p.Nk && qry < p.Nq && (!p.causal || key <= qry + shift);
-              const float pe = vis ? ex2_approx(__uint_as_float(sv[cc]) * p.scale_log2 - l2) : 0.f;
-              pr[e] = pe;
-              ds[e] = vis ? pe * (__uint_as_float(dpv[cc]) - dd) : 0.f;
+            float d0f, d1f;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(p0), __uint_as_float(p1)), t2), d0f, d1f);
+            uint32_t d0 = __float_as_uint(d0f), d1 = __float_as_uint(d1f);
+            if (!interior) {  // warp-uniform; hidden elements become +0 by a predicated select
+              keep_in_range(c, lo, hi, p0, d0);
+              keep_in_range(c + 1, lo, hi, p1, d1);
             }
-            pk[c / 2] = pack_bf16x2(pr[0], pr[1]);
-            dsk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+            pk[c / 2] = pack_bf16x2(__uint_as_float(p0), __uint_as_float(p1));
+            dsk[c / 2] = pack_bf16x2(__uint_as_float(d0), __uint_as_float(d1));
           }
         }
         // bf16 P^T (dK/dV pass) over this half's own first 16 S columns, bf16
@@ -514,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&sm.p_full[b]);
       }
       if (!ok) break;
-      if (!KV && unit_of(round + 1) < n_units && !(ok = prologue(round + 1, nxt_lse2, nxt_d))) break;
+      if (!KV && unit_of(round + 1) < n_units && !(ok = prologue(round + 1, nxt_lse, nxt_d))) break;
       // -------------------------------------------------------- epilogue
       if (n > 0) {
         if (!(ok = __all_sync(0xffffffffu, bwd_wait(&sm.acc_done, acc_units & 1, p, &sm.abort_flag)))) break;
@@ -544,12 +606,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // dK/dV pass: a = 0 is dV, a = 1 is dK (times scale); dQ pass: dQ (times scale)
           const float mul = (KV && a == 0) ? 1.f : p.scale;
-          const int lim = KV ? p.Nk : p.Nq;
-          if (row < lim) {
-            if (!KV || p.part == nullptr) {
-              const size_t plane = KV ? static_cast<size_t>(w.splane) : static_cast<size_t>(w.bh);
-              __nv_bfloat16* dst = (KV && a == 0) ? p.out1 : p.out0;
-              uint4* o = reinterpret_cast<uint4*>(dst + (plane * lim + row) * D + col0);
+          if constexpr (!KV) {
+            // This thread's half row of dQ, in bf16, into the O tile's slot
+            // where it read O (the tile's swizzled layout; rows past Nq are
+            // clipped by the store), once the previous unit's dQ has left it.
+            if (!(ok = __all_sync(0xffffffffu, bwd_wait(&sm.stat_free, units & 1, p, &sm.abort_flag)))) break;
+            const uint32_t stage = smem_u32(&sm.otile[0][0]);
+#pragma unroll
+            for (int c = 0; c < kHalf / 8; ++c) {
+              const int cc = half * (D / 16) + c;
+              const uint32_t off = (cc >> 3) * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + (((cc & 7) ^ (r & 7)) << 4);
+              st_shared_v4(stage + off,
+                           pack_bf16x2(__uint_as_float(v[8 * c]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
+                           pack_bf16x2(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
+                           pack_bf16x2(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
+                           pack_bf16x2(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.dq_staged);
+          } else if (row < p.Nk) {
+            if (p.part == nullptr) {
+              __nv_bfloat16* dst = a == 0 ? p.out1 : p.out0;
+              uint4* o = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(w.splane) * p.Nk + row) * D + col0);
 #pragma unroll
               for (int c = 0; c < kHalf / 8; ++c)
                 o[c] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * c]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
@@ -572,6 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (!ok) break;
       if (n > 0) ++acc_units;
       tiles += n;
       ++units;
@@ -646,6 +726,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
   p.scale_log2 = a.scale * kLog2e;
   constexpr int smem_kv = static_cast<int>(bwd_smem_bytes<D, true>());
   constexpr int smem_q = static_cast<int>(bwd_smem_bytes<D, false>());
+  static_assert(smem_kv <= 227 * 1024 && smem_q <= 227 * 1024, "shared memory per CTA");
   static std::atomic<int> set_kv[64] = {}, set_q[64] = {};
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(bwd_tc_kernel<D, true>), smem_kv, set_kv);
   if (e != cudaSuccess) return e;
@@ -663,7 +744,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     const long long units = static_cast<long long>(pq.n_tiles) * pq.n_bh;
     const long long grid = units < sms ? units : sms;
     bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, smem_q, stream>>>(
-        *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, *a.tm_o128, pq);
+        *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, *a.tm_o128, *a.tm_dq128, pq);
   }
   const int G = a.Hq / a.Hkv;
   if (a.Nk > 0) {
@@ -687,7 +768,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64,
-                           *a.tm_k128, pk);
+                           *a.tm_k128, *a.tm_k128, pk);
     if (e != cudaSuccess) return e;
     if (G > 1) {
       const long long n = static_cast<long long>(a.B) * a.Hkv * a.Nk * D;

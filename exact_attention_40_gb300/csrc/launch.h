@@ -128,7 +128,8 @@ struct BwdArgs {
   const CUtensorMap* tm_do128;
   const CUtensorMap* tm_k64;
   const CUtensorMap* tm_v64;
-  const CUtensorMap* tm_o128;  // out, 128-row boxes
+  const CUtensorMap* tm_o128;   // out, 128-row boxes
+  const CUtensorMap* tm_dq128;  // dq, 128-row boxes (TMA stores)
   const void* q;     // [B, Hq, Nq, d] bf16
   const void* k;     // [B, Hkv, Nk, d] bf16
   const void* v;
