@@ -497,8 +497,9 @@ int attn_rope_cache_write(void* q, const void* k, const void* v, const int32_t* 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128)) return 0;
   const size_t dsum = (static_cast<size_t>(B) * Hq * Nq * sizeof(float) + 15) / 16 * 16;
-  // with query heads sharing a KV head: fp32 dK and dV partials per query head
-  const size_t part = Hq > Hkv ? static_cast<size_t>(B) * Hq * Nk * d * sizeof(float) * 2 : 0;
+  // with query heads sharing a KV head: fp32 dK and dV partials per query
+  // head, from a 32-byte boundary (up to 16 bytes of slack after D)
+  const size_t part = Hq > Hkv ? static_cast<size_t>(B) * Hq * Nk * d * sizeof(float) * 2 + 16 : 0;
   return dsum + part;
 }
 
@@ -572,9 +573,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   a.dout = dout;
   a.lse = lse;
   a.dsum = static_cast<float*>(workspace);
-  a.part = Hq > Hkv ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                               (static_cast<size_t>(B) * Hq * Nq * sizeof(float) + 15) / 16 * 16)
-                    : nullptr;
+  if (Hq > Hkv) {
+    const uintptr_t p0 = reinterpret_cast<uintptr_t>(workspace) +
+                         (static_cast<size_t>(B) * Hq * Nq * sizeof(float) + 15) / 16 * 16;
+    a.part = reinterpret_cast<float*>((p0 + 31) & ~static_cast<uintptr_t>(31));  // 32-byte stores
+  } else {
+    a.part = nullptr;
+  }
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

@@ -75,7 +75,7 @@ struct alignas(1024) BwdSmem {
   uint8_t otile[KV ? 1 : D / 64][KV ? 16 : kStatSub];  // dQ pass: O, for D = rowsum(dO * O)
   float dpart[KV ? 1 : 2][KV ? 1 : kStatRows];          // dQ pass: D of each half of the columns
   uint64_t stat_full, stat_free, full[kStages], empty[kStages], s_full[2], p_full[2], acc_done, acc_free, fin;
-  uint64_t a_full, a_free;  // dQ pass: Q and dO rows in TMEM
+  uint64_t a_free;          // dQ pass: the unit's last products have read the TMEM copies of Q and dO
   uint64_t dpart_full;      // dQ pass: both halves' shares of D written
   uint64_t dq_staged;       // dQ pass: the tiles read (first phase), then each unit's dQ staged
   uint32_t tmem_base;
@@ -134,6 +134,39 @@ __device__ __forceinline__ void keep_in_range(int c, int lo, int hi, uint32_t& a
       "selp.b32 %0, %0, 0, q;\n\t"
       "selp.b32 %1, %1, 0, q;\n\t}"
       : "+r"(a), "+r"(b) : "r"(c), "r"(lo), "r"(hi));
+}
+
+// P and dS of one thread's 32 elements (one row of a warp's 32 x 32
+// block): p = 2^(s * scale * log2e - lse * log2e), ds = p (dp - D).  The
+// row's lse and D are per thread in the dQ pass (row = query) and per column
+// in the dK/dV pass (row = key), one column per lane there.  kMasked: the
+// elements outside [lo, hi) become +0.
+template <bool KV, bool kMasked>
+__device__ __forceinline__ void bwd_block(const uint32_t (&sv)[32], const uint32_t (&dpv)[32], float scale_log2,
+                                          float row_lse2, float row_d, float col_lse2, float col_d, int lo, int hi,
+                                          uint32_t (&pk)[16], uint32_t (&dsk)[16]) {
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const float l2a = KV ? __shfl_sync(0xffffffffu, col_lse2, c) : row_lse2;
+    const float l2b = KV ? __shfl_sync(0xffffffffu, col_lse2, c + 1) : row_lse2;
+    const float da = KV ? __shfl_sync(0xffffffffu, col_d, c) : row_d;
+    const float db = KV ? __shfl_sync(0xffffffffu, col_d, c + 1) : row_d;
+    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, f2_pack(-l2a, -l2b));
+    float x0, x1;
+    f2_unpack(x2, x0, x1);
+    uint32_t p0 = __float_as_uint(ex2_approx(x0)), p1 = __float_as_uint(ex2_approx(x1));
+    const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), f2_pack(-da, -db));
+    float d0f, d1f;
+    f2_unpack(f2_mul(f2_pack(__uint_as_float(p0), __uint_as_float(p1)), t2), d0f, d1f);
+    uint32_t d0 = __float_as_uint(d0f), d1 = __float_as_uint(d1f);
+    if constexpr (kMasked) {
+      keep_in_range(c, lo, hi, p0, d0);
+      keep_in_range(c + 1, lo, hi, p1, d1);
+    }
+    pk[c / 2] = pack_bf16x2(__uint_as_float(p0), __uint_as_float(p1));
+    dsk[c / 2] = pack_bf16x2(__uint_as_float(d0), __uint_as_float(d1));
+  }
 }
 
 template <bool KV>
@@ -206,14 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sm.stat_full, 1);
     // The stationary tiles are released by the MMA warp's commit after a
-    // unit's last products (dK/dV pass) or by the store warp (dQ pass): the
-    // O tile's slot then stages the previous unit's dQ, written by each
-    // elementwise warp over the bytes of O that it has read, and is free
-    // once the TMA store has read it.  The TMEM copies of Q and dO are
-    // filled by the elementwise warps and released by the MMA warp's commit
-    // after the unit's last products.
-    mbar_init(&sm.stat_free, 1);
-    mbar_init(&sm.a_full, 8);
+    // unit's last products (dK/dV pass), or (dQ pass) by two arrivals: the
+    // MMA warp's commit after its copies of Q and dO into TMEM, and the
+    // store warp's: the O tile's slot stages the previous unit's dQ, written
+    // by each elementwise warp over the bytes of O that it has read, and is
+    // free once the TMA store has read it.
+    mbar_init(&sm.stat_free, KV ? 1 : 2);
     mbar_init(&sm.a_free, 1);
     mbar_init(&sm.dpart_full, 8);
     mbar_init(&sm.dq_staged, 8);
@@ -353,9 +384,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = unit_of(round);
       if (u >= n_units) break;
       const int n = work_of<KV>(u, p).count;
-      // dK/dV pass: the K and V tiles in shared memory; dQ pass: the Q and dO rows in TMEM
-      if (!(ok = wait_all(KV ? &sm.stat_full : &sm.a_full, units & 1))) break;
+      // the stationary tiles in shared memory
+      if (!(ok = wait_all(&sm.stat_full, units & 1))) break;
+      // dQ pass: once the previous unit's products have read them, the TMEM
+      // copies of Q and dO are overwritten with this unit's (A of S and dP)
+      if (!KV && units > 0 && !(ok = wait_all(&sm.a_free, (units - 1) & 1))) break;
       tc_fence_after_sync();
+      if constexpr (!KV) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk / 4) * (kStatSub / 16) + (kk % 4) * 2;
+          tmem_cp_128x256b_warp(tmem + kQCol + kk * 8, d_s0 + oa);
+          tmem_cp_128x256b_warp(tmem + kQCol + D / 2 + kk * 8, d_s1 + oa);
+        }
+        umma_commit_warp(&sm.stat_free);  // the copies have read the Q and dO tiles
+        mma_issued = true;
+      }
       for (int i = 0; ok && i < n; ++i) {
         const int t = tiles + i;
         if (!(ok = wait_all(&sm.full[t % kStages], (t / kStages) & 1))) break;
@@ -411,13 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int units = 0, tiles = 0, acc_units = 0;
     // dQ pass, once per unit and before the previous unit's epilogue: each
-    // half of the warps reads its half of the columns of this thread's dO, O
-    // and Q rows (rows past Nq read as zero) and forms its share of D; the
-    // tiles are released as soon as they are read, so the next unit's can
-    // load meanwhile.  Once the previous unit's products have read them, the
-    // Q and dO halves go into the TMEM A operands; the two shares of D meet
-    // in shared memory (first half + second half, the same sum in both) and
-    // the first half writes D for the dK/dV pass.
+    // half of the warps reads its half of the columns of this thread's dO
+    // and O rows (rows past Nq read as zero) and forms its share of D; the
+    // two shares meet in shared memory (first half + second half, the same
+    // sum in both halves) and the first half writes D for the dK/dV pass.
+    // (The MMA warp copies the unit's Q and dO tiles into TMEM itself.)
     float nxt_lse = 0.f, nxt_d = 0.f;
     auto prologue = [&](int rnd, float& lse_out, float& d_out) -> bool {
       const Work wq = work_of<KV>(unit_of(rnd), p);
@@ -425,52 +467,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t l0 = static_cast<size_t>(wq.bh) * p.Nq;
       lse_out = qrow < p.Nq ? p.lse[l0 + qrow] : 0.f;  // natural log; scaled where it is used
       if (!__all_sync(0xffffffffu, bwd_wait(&sm.stat_full, rnd & 1, p, &sm.abort_flag))) return false;
-      const uint8_t* qb = &sm.stat[0][0][0];
       const uint8_t* dob = &sm.stat[1][0][0];
       const uint8_t* ob = &sm.otile[0][0];
       float acc = 0.f;
-      uint32_t qv[D / 4], dv[D / 4];  // elements [half * D / 2, + D / 2) of the row, two a word
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
         const int cc = half * (D / 16) + c;  // 16-byte chunk of the row
         const uint32_t off = (cc >> 3) * kStatSub + (r >> 3) * 1024 + (r & 7) * 128 + (((cc & 7) ^ (r & 7)) << 4);
-        const uint4 a = *reinterpret_cast<const uint4*>(qb + off);
-        const uint4 b = *reinterpret_cast<const uint4*>(dob + off);
         float fo[8], fd[8];
         unpack_bf16x8(*reinterpret_cast<const uint4*>(ob + off), fo);
-        unpack_bf16x8(b, fd);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(dob + off), fd);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc = fmaf(fd[e], fo[e], acc);
-        qv[4 * c] = a.x; qv[4 * c + 1] = a.y; qv[4 * c + 2] = a.z; qv[4 * c + 3] = a.w;
-        dv[4 * c] = b.x; dv[4 * c + 1] = b.y; dv[4 * c + 2] = b.z; dv[4 * c + 3] = b.w;
       }
-      // The first unit's tiles are free once read; a later unit's once the
-      // previous unit's dQ, staged after this read, has been stored.
-      __syncwarp();
-      if (rnd == 0 && lane == 0) mbar_arrive(&sm.dq_staged);
-      // After a_free (which follows a_full) every warp has read the previous
-      // unit's shares of D.
-      if (rnd > 0 && !__all_sync(0xffffffffu, bwd_wait(&sm.a_free, (rnd - 1) & 1, p, &sm.abort_flag))) return false;
+      // Every warp has read the previous unit's shares once phase rnd - 1
+      // of dq_staged has completed (each warp arrives there after its read).
+      if (rnd > 0 && !__all_sync(0xffffffffu, bwd_wait(&sm.dq_staged, (rnd - 1) & 1, p, &sm.abort_flag))) return false;
       sm.dpart[half][r] = acc;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.dpart_full);
-      tc_fence_after_sync();
-      const uint32_t qc = t_lane + kQCol + static_cast<uint32_t>(half * (D / 4));
-      if constexpr (D == 128) {
-        tmem_st_32x32b_x32(qc, *reinterpret_cast<const uint32_t(*)[32]>(&qv[0]));
-        tmem_st_32x32b_x32(qc + D / 2, *reinterpret_cast<const uint32_t(*)[32]>(&dv[0]));
-      } else {
-        tmem_st_32x32b_x16(qc, *reinterpret_cast<const uint32_t(*)[16]>(&qv[0]));
-        tmem_st_32x32b_x16(qc + D / 2, *reinterpret_cast<const uint32_t(*)[16]>(&dv[0]));
-      }
-      tmem_st_wait();
-      // Both shares are read before a_full: the next unit's shares are
-      // written only after a_free, which follows a_full.
       if (!__all_sync(0xffffffffu, bwd_wait(&sm.dpart_full, rnd & 1, p, &sm.abort_flag))) return false;
       const float dd = sm.dpart[0][r] + sm.dpart[1][r];
-      tc_fence_before_sync();
+      // The first unit's tiles are free (for this warp) once read; a later
+      // unit's once the previous unit's dQ, staged after this read, has been
+      // stored.
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.a_full);
+      if (rnd == 0 && lane == 0) mbar_arrive(&sm.dq_staged);
       d_out = dd;
       if (half == 0 && qrow < p.Nq) p.dsum[l0 + qrow] = dd;
       return true;
@@ -539,28 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo = static_cast<int>(max(0ll, min(l, 32ll)));
             hi = static_cast<int>(max(0ll, min(h, 32ll)));
           }
-          const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float l2a = KV ? __shfl_sync(0xffffffffu, col_lse2, c) : row_lse2;
-            const float l2b = KV ? __shfl_sync(0xffffffffu, col_lse2, c + 1) : row_lse2;
-            const float da = KV ? __shfl_sync(0xffffffffu, col_d, c) : row_d;
-            const float db = KV ? __shfl_sync(0xffffffffu, col_d, c + 1) : row_d;
-            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, f2_pack(-l2a, -l2b));
-            float x0, x1;
-            f2_unpack(x2, x0, x1);
-            uint32_t p0 = __float_as_uint(ex2_approx(x0)), p1 = __float_as_uint(ex2_approx(x1));
-            const uint64_t t2 = f2_add(f2_pack(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])), f2_pack(-da, -db));
-            float d0f, d1f;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(p0), __uint_as_float(p1)), t2), d0f, d1f);
-            uint32_t d0 = __float_as_uint(d0f), d1 = __float_as_uint(d1f);
-            if (!interior) {  // warp-uniform; hidden elements become +0 by a predicated select
-              keep_in_range(c, lo, hi, p0, d0);
-              keep_in_range(c + 1, lo, hi, p1, d1);
-            }
-            pk[c / 2] = pack_bf16x2(__uint_as_float(p0), __uint_as_float(p1));
-            dsk[c / 2] = pack_bf16x2(__uint_as_float(d0), __uint_as_float(d1));
-          }
+          if (interior)
+            bwd_block<KV, false>(sv, dpv, p.scale_log2, row_lse2, row_d, col_lse2, col_d, 0, 32, pk, dsk);
+          else
+            bwd_block<KV, true>(sv, dpv, p.scale_log2, row_lse2, row_d, col_lse2, col_d, lo, hi, pk, dsk);
         }
         // bf16 P^T (dK/dV pass) over this half's own first 16 S columns, bf16
         // dS over its own first 16 dP columns (dK/dV pass) or S columns (dQ pass)
@@ -642,11 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int g = (w.bh % p.Hq) % G;
               float* dst = p.part + static_cast<size_t>(a == 0 ? G + g : g) * plane_elems +
                            (static_cast<size_t>(w.splane) * p.Nk + row) * D + col0;
-              float4* o = reinterpret_cast<float4*>(dst);
+              // 32-byte stores (the partials start on a 32-byte boundary)
 #pragma unroll
-              for (int c = 0; c < kHalf / 4; ++c)
-                o[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                   __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+              for (int c = 0; c < kHalf / 8; ++c)
+                st_global_v8(dst + 8 * c, &v[8 * c]);
             }
           }
         }

@@ -261,6 +261,21 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
       : "memory");
 }
 
+// Copy a 128-row x 256-bit matrix from shared memory (described by a
+// matrix descriptor, as for an MMA operand) into TMEM lanes 0-127, eight
+// consecutive 32-bit columns from taddr.  Asynchronous: an MMA issued later
+// by the same thread reads the copy; an MMA issued earlier may still be
+// reading the columns, so the issuer waits for its commit first.  One
+// elected lane of the calling warp issues.
+__device__ __forceinline__ void tmem_cp_128x256b_warp(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -426,6 +441,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
                "r"(d)
+               : "memory");
+}
+
+// Eight 32-bit words to global memory in one 32-byte store; p 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                : "memory");
 }
 
