@@ -116,6 +116,34 @@ int tensor_map(int dev, const void* ptr, int d, long long rows, long long planes
   return EXATTN_OK;
 }
 
+// Descriptor of the backward's fp32 (lse * log2 e, D) pairs [planes][nq_pad][2]
+// (nq_pad = nq rounded up to even, so rows start on 16-byte boundaries),
+// viewed as [planes][1][2 nq] and loaded in boxes of 64 pairs; pairs past nq
+// read as zero.  Cached and copied like tensor_map's.
+int pair_map(int dev, const void* ptr, long long nq, long long planes, CUtensorMap* out) {
+  const MapKey key{reinterpret_cast<uintptr_t>(ptr), 0, nq, planes, 64};  // d = 0: never a bf16 map
+  auto& cache = g_maps[dev];
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return EXATTN_OK;
+  }
+  if (cache.size() >= kMapCacheMax) cache.clear();
+  CUtensorMap m;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>((nq + 1) / 2 * 2) * 8;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(2 * nq), 1, static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {row_bytes, row_bytes};
+  cuuint32_t box[3] = {128, 1, 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides,
+                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return EXATTN_ERR_CUDA;
+  cache.emplace(key, m);
+  *out = m;
+  return EXATTN_OK;
+}
+
 // One warp waits on a barrier with arrival count 2 that only ever sees one
 // arrival, so the phase never completes and the bounded wait must expire.
 __global__ void expire_wait_kernel(unsigned int* status, unsigned long long budget_ns) {
@@ -496,11 +524,12 @@ int attn_rope_cache_write(void* q, const void* k, const void* v, const int32_t* 
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128)) return 0;
-  const size_t dsum = (static_cast<size_t>(B) * Hq * Nq * sizeof(float) + 15) / 16 * 16;
+  // fp32 (lse * log2 e, D) pairs per query row, rows padded to an even count
+  const size_t pairs = static_cast<size_t>(B) * Hq * ((static_cast<size_t>(Nq) + 1) / 2 * 2) * 2 * sizeof(float);
   // with query heads sharing a KV head: fp32 dK and dV partials per query
-  // head, from a 32-byte boundary (up to 16 bytes of slack after D)
+  // head, from a 32-byte boundary (up to 16 bytes of slack after the pairs)
   const size_t part = Hq > Hkv ? static_cast<size_t>(B) * Hq * Nk * d * sizeof(float) * 2 + 16 : 0;
-  return dsum + part;
+  return pairs + part;
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
@@ -530,7 +559,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   if (need > 0 && !aligned16(workspace)) return EXATTN_ERR_ALIGNMENT;
   exattn::BwdArgs a;
   exattn::DeviceGuard g;
-  CUtensorMap maps[10];  // copied into the launches' parameters
+  CUtensorMap maps[11];  // copied into the launches' parameters
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int dev;
@@ -552,7 +581,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
       if ((rc = tensor_map(dev, v, d, Nk, pk, &maps[7], 64)) != EXATTN_OK) return rc;
     }
     // an empty side has no tiles to load: its maps are stand-ins, never used
+    if (Nq > 0 && Nk > 0 && (rc = pair_map(dev, workspace, Nq, pq, &maps[10])) != EXATTN_OK) return rc;
     if (Nq == 0) maps[0] = maps[1] = maps[4] = maps[5] = maps[8] = maps[9] = maps[2];
+    if (Nq == 0 || Nk == 0) maps[10] = maps[0];
     if (Nk == 0) maps[2] = maps[3] = maps[6] = maps[7] = maps[0];
   }
   g.wait_ns = wait_budget_ns();
@@ -566,16 +597,17 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   a.tm_v64 = &maps[7];
   a.tm_o128 = &maps[8];
   a.tm_dq128 = &maps[9];
+  a.tm_ldp = &maps[10];
   a.q = q;
   a.k = k;
   a.v = v;
   a.out = out;
   a.dout = dout;
   a.lse = lse;
-  a.dsum = static_cast<float*>(workspace);
+  a.ldp = static_cast<float*>(workspace);
   if (Hq > Hkv) {
     const uintptr_t p0 = reinterpret_cast<uintptr_t>(workspace) +
-                         (static_cast<size_t>(B) * Hq * Nq * sizeof(float) + 15) / 16 * 16;
+                         static_cast<size_t>(B) * Hq * ((static_cast<size_t>(Nq) + 1) / 2 * 2) * 2 * sizeof(float);
     a.part = reinterpret_cast<float*>((p0 + 31) & ~static_cast<uintptr_t>(31));  // 32-byte stores
   } else {
     a.part = nullptr;

@@ -74,6 +74,7 @@ struct alignas(1024) BwdSmem {
   uint8_t ring[kStages][2][D / 64][kStreamSub];   // Q, dO (dK/dV pass) or K, V (dQ pass)
   uint8_t otile[KV ? 1 : D / 64][KV ? 16 : kStatSub];  // dQ pass: O, for D = rowsum(dO * O)
   float dpart[KV ? 1 : 2][KV ? 1 : kStatRows];          // dQ pass: D of each half of the columns
+  alignas(128) float ldp[KV ? kStages : 1][KV ? 2 * kStreamRows : 4];  // dK/dV pass: (lse * log2 e, D) of the streamed queries
   uint64_t stat_full, stat_free, full[kStages], empty[kStages], s_full[2], p_full[2], acc_done, acc_free, fin;
   uint64_t a_free;          // dQ pass: the unit's last products have read the TMEM copies of Q and dO
   uint64_t dpart_full;      // dQ pass: both halves' shares of D written
@@ -84,13 +85,13 @@ struct alignas(1024) BwdSmem {
 
 struct BwdParams {
   const float* lse;      // [B*Hq, Nq], natural log
-  float* dsum;           // [B*Hq, Nq]: D, written by the dQ pass, read by the dK/dV pass
+  float* ldp;            // [B*Hq][nq_pad][2]: (lse * log2 e, D), written by the dQ pass, loaded by the dK/dV pass
   __nv_bfloat16* out0;   // dK (dK/dV pass, one query head per KV head) or dQ
   __nv_bfloat16* out1;   // dV (dK/dV pass, one query head per KV head)
   float* part;           // dK/dV pass with GQA: partials [G][B*Hkv][Nk][D] of dK, then of dV
   unsigned int* status;
   unsigned long long wait_ns;
-  int Hq, Hkv, Nq, Nk, causal, n_bh, n_tiles;
+  int Hq, Hkv, Nq, Nk, causal, n_bh, n_tiles, nq_pad;
   float scale, scale_log2;
 };
 
@@ -139,19 +140,24 @@ __device__ __forceinline__ void keep_in_range(int c, int lo, int hi, uint32_t& a
 // P and dS of one thread's 32 elements (one row of a warp's 32 x 32
 // block): p = 2^(s * scale * log2e - lse * log2e), ds = p (dp - D).  The
 // row's lse and D are per thread in the dQ pass (row = query) and per column
-// in the dK/dV pass (row = key), one column per lane there.  kMasked: the
-// elements outside [lo, hi) become +0.
+// in the dK/dV pass (row = key): there the (lse * log2e, D) pairs of the 32
+// columns, in shared memory, read as broadcasts.  kMasked: the elements
+// outside [lo, hi) become +0.
 template <bool KV, bool kMasked>
 __device__ __forceinline__ void bwd_block(const uint32_t (&sv)[32], const uint32_t (&dpv)[32], float scale_log2,
-                                          float row_lse2, float row_d, float col_lse2, float col_d, int lo, int hi,
+                                          float row_lse2, float row_d, const float* cols, int lo, int hi,
                                           uint32_t (&pk)[16], uint32_t (&dsk)[16]) {
   const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
-    const float l2a = KV ? __shfl_sync(0xffffffffu, col_lse2, c) : row_lse2;
-    const float l2b = KV ? __shfl_sync(0xffffffffu, col_lse2, c + 1) : row_lse2;
-    const float da = KV ? __shfl_sync(0xffffffffu, col_d, c) : row_d;
-    const float db = KV ? __shfl_sync(0xffffffffu, col_d, c + 1) : row_d;
+    float l2a = row_lse2, l2b = row_lse2, da = row_d, db = row_d;
+    if constexpr (KV) {
+      const float4 q = *reinterpret_cast<const float4*>(cols + 2 * c);
+      l2a = q.x;
+      da = q.y;
+      l2b = q.z;
+      db = q.w;
+    }
     const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, f2_pack(-l2a, -l2b));
     float x0, x1;
     f2_unpack(x2, x0, x1);
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_s1,
                   const __grid_constant__ CUtensorMap tm_r0, const __grid_constant__ CUtensorMap tm_r1,
                   const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dq,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_ldp, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   BwdSmem<D, KV>& sm = *reinterpret_cast<BwdSmem<D, KV>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -236,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!KV) {
       tma_prefetch_desc(&tm_o);
       tma_prefetch_desc(&tm_dq);
+    } else {
+      tma_prefetch_desc(&tm_ldp);
     }
     mbar_init(&sm.stat_full, 1);
     // The stationary tiles are released by the MMA warp's commit after a
@@ -281,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();  // streamed tiles are re-read by other CTAs
       bool ok = true;
+      bool dq_done = false;  // dK/dV pass: the dQ pass (which writes lse and D pairs) has completed
       for (int round = 0; ok; ++round) {
         const int u = unit_of(round);
         if (u >= n_units) break;
@@ -300,11 +309,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = t % kStages;
           if (t >= kStages && !(ok = bwd_wait(&sm.empty[s], ((t / kStages) - 1) & 1, p, &sm.abort_flag))) break;
           const int row = (w.first + i) * kStreamRows;
-          mbar_arrive_expect_tx(&sm.full[s], 2 * D * kStreamRows * 2);
+          mbar_arrive_expect_tx(&sm.full[s], 2 * D * kStreamRows * 2 + (KV ? 2 * kStreamRows * 4 : 0));
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d_hint(sm.ring[s][0][c], &tm_r0, &sm.full[s], c * 64, row, w.rplane, keep);
             tma_load_3d_hint(sm.ring[s][1][c], &tm_r1, &sm.full[s], c * 64, row, w.rplane, keep);
+          }
+          if constexpr (KV) {
+            // the streamed queries' (lse * log2 e, D): written by the dQ pass,
+            // which may still be finishing when this grid starts
+            if (!dq_done) {
+              asm volatile("griddepcontrol.wait;" ::: "memory");
+              asm volatile("fence.proxy.async.global;" ::: "memory");  // for the TMA reads that follow
+              dq_done = true;
+            }
+            tma_load_3d(sm.ldp[s], &tm_ldp, &sm.full[s], 2 * row, 0, w.rplane);
           }
           loads_issued = t + 1;
         }
@@ -444,9 +463,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise warps
-    // dK/dV pass: D comes from the dQ pass, which may still be finishing
-    // when this grid starts (its copies and products need nothing from it).
-    if (KV) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int quarter = warp & 3;  // TMEM lanes 32 quarter ..
     const int half = warp >> 2;    // columns 32 half .. of the 64 streamed rows
     const int r = quarter * 32 + lane;
@@ -494,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (rnd == 0 && lane == 0) mbar_arrive(&sm.dq_staged);
       d_out = dd;
-      if (half == 0 && qrow < p.Nq) p.dsum[l0 + qrow] = dd;
+      if (half == 0 && qrow < p.Nq)
+        reinterpret_cast<float2*>(p.ldp)[static_cast<size_t>(wq.bh) * p.nq_pad + qrow] = make_float2(lse_out * kLog2e, dd);
       return true;
     };
     for (int round = 0; ok; ++round) {
@@ -503,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Work w = work_of<KV>(u, p);
       const int n = w.count;
       const int row = w.srow + r;  // key (dK/dV pass) or query row (dQ pass) of this thread
-      const size_t lrow0 = static_cast<size_t>(w.bh) * p.Nq;
       float row_lse2 = 0.f, row_d = 0.f;
       if constexpr (!KV) {
         if (round == 0 && !(ok = prologue(0, nxt_lse, nxt_d))) break;
@@ -514,11 +530,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = tiles + i;
         const int b = t & 1;
         const int c0 = (w.first + i) * kStreamRows + half * 32;  // first streamed row of this half
-        float col_lse2 = 0.f, col_d = 0.f;  // dK/dV pass: query c0 + lane
-        if (KV && c0 + lane < p.Nq) {
-          col_lse2 = p.lse[lrow0 + c0 + lane] * kLog2e;
-          col_d = p.dsum[lrow0 + c0 + lane];
-        }
         // This warp's 32 x 32 block: rows r_lo.. (keys in the dK/dV pass,
         // queries in the dQ pass), streamed columns c_lo..
         const long long r_lo = w.srow + quarter * 32, r_hi = r_lo + 31;
@@ -561,10 +572,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo = static_cast<int>(max(0ll, min(l, 32ll)));
             hi = static_cast<int>(max(0ll, min(h, 32ll)));
           }
+          // dK/dV pass: this half's 32 (lse * log2 e, D) pairs, loaded with
+          // the stage's tiles (the products waited for them; so does this warp)
+          const float* cols = &sm.ldp[0][0];
+          if constexpr (KV) {
+            const int s = t % kStages;
+            if (!(ok = __all_sync(0xffffffffu, bwd_wait(&sm.full[s], (t / kStages) & 1, p, &sm.abort_flag)))) break;
+            cols = &sm.ldp[s][2 * 32 * half];
+          }
           if (interior)
-            bwd_block<KV, false>(sv, dpv, p.scale_log2, row_lse2, row_d, col_lse2, col_d, 0, 32, pk, dsk);
+            bwd_block<KV, false>(sv, dpv, p.scale_log2, row_lse2, row_d, cols, 0, 32, pk, dsk);
           else
-            bwd_block<KV, true>(sv, dpv, p.scale_log2, row_lse2, row_d, col_lse2, col_d, lo, hi, pk, dsk);
+            bwd_block<KV, true>(sv, dpv, p.scale_log2, row_lse2, row_d, cols, lo, hi, pk, dsk);
         }
         // bf16 P^T (dK/dV pass) over this half's own first 16 S columns, bf16
         // dS over its own first 16 dP columns (dK/dV pass) or S columns (dQ pass)
@@ -716,7 +735,7 @@ template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t stream) {
   BwdParams p;
   p.lse = a.lse;
-  p.dsum = a.dsum;
+  p.ldp = a.ldp;
   p.status = g.status;
   p.wait_ns = g.wait_ns;
   p.Hq = a.Hq;
@@ -727,6 +746,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
   p.n_bh = a.B * a.Hq;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  p.nq_pad = (a.Nq + 1) / 2 * 2;
   constexpr int smem_kv = static_cast<int>(bwd_smem_bytes<D, true>());
   constexpr int smem_q = static_cast<int>(bwd_smem_bytes<D, false>());
   static_assert(smem_kv <= 227 * 1024 && smem_q <= 227 * 1024, "shared memory per CTA");
@@ -747,7 +767,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     const long long units = static_cast<long long>(pq.n_tiles) * pq.n_bh;
     const long long grid = units < sms ? units : sms;
     bwd_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, smem_q, stream>>>(
-        *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, *a.tm_o128, *a.tm_dq128, pq);
+        *a.tm_q128, *a.tm_do128, *a.tm_k64, *a.tm_v64, *a.tm_o128, *a.tm_dq128, *a.tm_ldp, pq);
   }
   const int G = a.Hq / a.Hkv;
   if (a.Nk > 0) {
@@ -771,7 +791,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const DeviceGuard& g, cudaStream_t st
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, true>, *a.tm_k128, *a.tm_v128, *a.tm_q64, *a.tm_do64,
-                           *a.tm_k128, *a.tm_k128, pk);
+                           *a.tm_k128, *a.tm_k128, *a.tm_ldp, pk);
     if (e != cudaSuccess) return e;
     if (G > 1) {
       const long long n = static_cast<long long>(a.B) * a.Hkv * a.Nk * D;

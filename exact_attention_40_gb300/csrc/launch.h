@@ -130,13 +130,14 @@ struct BwdArgs {
   const CUtensorMap* tm_v64;
   const CUtensorMap* tm_o128;   // out, 128-row boxes
   const CUtensorMap* tm_dq128;  // dq, 128-row boxes (TMA stores)
+  const CUtensorMap* tm_ldp;    // ldp as [B*Hq][1][2 Nq] fp32, 64-pair boxes
   const void* q;     // [B, Hq, Nq, d] bf16
   const void* k;     // [B, Hkv, Nk, d] bf16
   const void* v;
   const void* out;   // forward output [B, Hq, Nq, d] bf16
   const void* dout;  // [B, Hq, Nq, d] bf16
   const float* lse;  // forward log-sum-exp [B, Hq, Nq]
-  float* dsum;       // workspace: D [B, Hq, Nq]
+  float* ldp;        // workspace: (lse * log2 e, D) pairs [B*Hq][Nq rounded up to even][2]
   float* part;       // workspace (Hq > Hkv): dK, dV partials per query head, fp32
   void* dq;          // [B, Hq, Nq, d] bf16
   void* dk;          // [B, Hkv, Nk, d] bf16

@@ -182,11 +182,11 @@ int attn_add_rms_norm(const void* x, const void* residual, const void* weight, v
                       void* residual_out, int n_rows, int hidden, float eps, void* stream);
 
 /*
- * Bytes of caller-provided device workspace attn_bwd needs: D (fp32
- * [B, Hq, Nq], rounded up to 16 bytes) and, when query heads share a KV head
- * (Hq > Hkv), room for fp32 dK and dV partials per query head
- * ([2][B*Hq][Nk][d], placed on the next 32-byte boundary: 16 bytes of
- * slack).
+ * Bytes of caller-provided device workspace attn_bwd needs: fp32
+ * (lse * log2 e, D) pairs per query row ([B*Hq][Nq rounded up to even][2])
+ * and, when query heads share a KV head (Hq > Hkv), room for fp32 dK and dV
+ * partials per query head ([2][B*Hq][Nk][d], placed on the next 32-byte
+ * boundary: 16 bytes of slack).
  * Returns 0 for invalid arguments (or nothing to store).
  */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);

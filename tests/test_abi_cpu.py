@@ -238,11 +238,12 @@ def bwd(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, do=FAKE, lse=FAKE, dq=FAKE + 16, 
 
 
 def test_bwd_rejections_and_workspace(lib):
-    assert lib.lib.attn_bwd_workspace_bytes(2, 4, 4, 10, 7, 64) == 2 * 4 * 10 * 4
-    assert lib.lib.attn_bwd_workspace_bytes(1, 1, 1, 3, 5, 128) == 16
+    # fp32 (lse * log2 e, D) pairs per query row, rows padded to an even count
+    assert lib.lib.attn_bwd_workspace_bytes(2, 4, 4, 10, 7, 64) == 2 * 4 * 10 * 8
+    assert lib.lib.attn_bwd_workspace_bytes(1, 1, 1, 3, 5, 128) == 4 * 8
     # query heads sharing a KV head: fp32 dK, dV partials per query head, from a
     # 32-byte boundary of a 16-byte aligned workspace (16 bytes of slack)
-    assert lib.lib.attn_bwd_workspace_bytes(1, 4, 2, 8, 6, 64) == 4 * 8 * 4 + 4 * 6 * 64 * 4 * 2 + 16
+    assert lib.lib.attn_bwd_workspace_bytes(1, 4, 2, 8, 6, 64) == 4 * 8 * 8 + 4 * 6 * 64 * 4 * 2 + 16
     assert lib.lib.attn_bwd_workspace_bytes(1, 4, 3, 8, 6, 64) == 0
     assert bwd(lib, d=96) == 2
     assert bwd(lib, Hq=3, Hkv=2) == 1

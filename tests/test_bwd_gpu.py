@@ -84,6 +84,12 @@ def test_unequal_lengths(env, Nq, Nk):
     run(env, 82, 2, 2, 1, Nq, Nk, 128, True)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_odd_lengths(env, causal):
+    # odd Nq: the per-row (lse, D) pairs of each head sit in rows padded to an even count
+    run(env, 84, 2, 4, 2, 77, 93, 64, causal)
+
+
 def test_llama_heads_causal(env):
     # a quarter of the Llama-3-8B heads (8 query, 2 key/value) at 2048 tokens
     run(env, 83, 1, 8, 2, 2048, 2048, 128, True)
