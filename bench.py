@@ -44,8 +44,8 @@ WORKLOAD = ("prefill llama3_8b_causal (B1 Hq32 Hkv8 Nq=Nk=2048 d128 causal) + "
 METRIC = "attn fwd TFLOP/s & % BF16 tensor peak; paged decode GB/s & % HBM peak"
 
 
-BWD_KERNELS = ("dQ (tcgen05, Q and dO as TMEM operands, also forms D) + dK/dV (tcgen05), both persistent; "
-               "GQA partials summed in head order")
+BWD_KERNELS = ("dQ (tcgen05; Q and dO copied into TMEM by tcgen05.cp; forms D; dQ leaves by TMA store) + "
+               "dK/dV (tcgen05; per-query lse and D staged by TMA), both persistent; GQA partials summed in head order")
 
 # Dense bf16 tensor rate of one SM: one M128 N128 K16 tcgen05.mma (524,288
 # FLOP) per 64 cycles.  A stand-alone loop issuing the prefill's MMAs back to
