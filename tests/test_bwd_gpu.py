@@ -131,3 +131,11 @@ def test_group_sizes(env, Hq, Hkv):
     # groups of 8 and 3 (fp32 partials and their sum in head order) and 1
     # (dK, dV written directly)
     run(env, 86, 1, Hq, Hkv, 200, 200, 64, True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_small_units(env, causal):
+    # 256 (batch, head) planes of 256 rows: 512 units of one to four tiles in
+    # each pass, so every CTA runs three or four unit changes (stationary
+    # copies, D shares, dQ staging, accumulator hand-off) back to back
+    run(env, 87, 8, 32, 8, 256, 256, 128, causal)
