@@ -9,27 +9,30 @@
 // P and dS are recomputed tile by tile from Q, K and the saved LSE, never
 // stored.  Kernels (no atomics, deterministic), in launch order:
 //   * bwd_tc_kernel<D, false> (dQ pass): a unit is a 128-row query tile of
-//     one head.  Its Q, dO and O tiles come into shared memory; the
-//     elementwise warps form D for their rows from dO and O (each half of
-//     the warps over its half of the columns; written for the dK/dV pass)
-//     and copy the Q and dO rows into TMEM, where they are the A operands of
-//     S = Q K^T and dP = dO V^T (M128 N64, B = the streamed 64-key K and V
-//     tiles of a 4-stage TMA ring), so the tensor core reads only the
-//     streamed tiles from shared memory.  dS = P (dP - D) goes back to TMEM
-//     as bf16 and dQ += dS K accumulates in TMEM.  dQ leaves through the O
-//     tile's slot: staged there in bf16 and written by a TMA store;
+//     one head.  Its Q, dO and O tiles come into shared memory; the MMA warp
+//     copies Q and dO into TMEM (tcgen05.cp), where they are the A operands
+//     of S = Q K^T and dP = dO V^T (M128 N64, B = the streamed 64-key K and
+//     V tiles of a 4-stage TMA ring), so the tensor core reads only the
+//     streamed tiles from shared memory.  The elementwise warps form D for
+//     their rows from dO and O (each half of the warps over its half of the
+//     columns) and write (lse * log2 e, D) for the dK/dV pass.  dS =
+//     P (dP - D) goes back to TMEM as bf16 and dQ += dS K accumulates in
+//     TMEM.  dQ leaves through the O tile's slot: staged there in bf16 and
+//     written by a TMA store;
 //   * bwd_tc_kernel<D, true> (dK/dV pass): a unit is a 128-key block of one
 //     query head.  K and V stay in shared memory; the 64-row query tiles of
-//     that head that the mask leaves stream through the ring.  Per tile the
-//     tensor core forms S^T = K Q^T and dP^T = V dO^T (M128 N64) into a
-//     double-buffered pair of TMEM regions; eight elementwise warps (thread =
-//     key = TMEM lane, two warps per lane quarter, one per half of the query
-//     columns) turn them into P^T and dS^T = P^T (dP^T - D), written back to
-//     TMEM as bf16 over their own fp32 columns; then dV += P^T dO and
-//     dK += dS^T Q accumulate in TMEM with A read from TMEM and dO, Q
-//     MN-major from shared memory.  With one query head per KV head it
-//     writes dK, dV directly; with GQA each query head writes fp32 partials
-//     that bwd_reduce_kernel sums in head order.
+//     that head that the mask leaves stream through the ring, each with its
+//     queries' (lse * log2 e, D) pairs.  Per tile the tensor core forms
+//     S^T = K Q^T and dP^T = V dO^T (M128 N64) into a double-buffered pair
+//     of TMEM regions; eight elementwise warps (thread = key = TMEM lane, two
+//     warps per lane quarter, one per half of the query columns, the pairs
+//     read as shared-memory broadcasts) turn them into P^T and
+//     dS^T = P^T (dP^T - D), written back to TMEM as bf16 over their own
+//     fp32 columns; then dV += P^T dO and dK += dS^T Q accumulate in TMEM
+//     with A read from TMEM and dO, Q MN-major from shared memory.  With one
+//     query head per KV head it writes dK, dV directly; with GQA each query
+//     head writes fp32 partials (32-byte stores) that bwd_reduce_kernel sums
+//     in head order.
 // The dK/dV pass and the GQA sum are programmatic dependent launches: each
 // grid may start on SMs that the previous one has left while that one's
 // last CTAs finish, and waits for its results where it reads them.
@@ -41,9 +44,9 @@
 // products are queued before the previous unit's epilogue is done.
 // Warp roles (352 threads): warps 0-7 elementwise, warp 8 TMA producer,
 // warp 9 tcgen05 issuer (warp-uniform loop, one elected lane issues) and
-// owner of the TMEM allocation, warp 10 the dQ pass's TMA stores.  Every wait is bounded; a wait that runs
-// out sets the device status word, drains what is in flight, frees TMEM and
-// returns.
+// owner of the TMEM allocation, warp 10 the dQ pass's TMA stores.  Every
+// wait is bounded; a wait that runs out sets the device status word, drains
+// what is in flight, frees TMEM and returns.
 #include <cuda_bf16.h>
 
 #include "launch.h"
