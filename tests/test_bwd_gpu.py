@@ -134,8 +134,10 @@ def test_group_sizes(env, Hq, Hkv):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_many_small_units(env, causal):
-    # 256 (batch, head) planes of 256 rows: 512 units of one to four tiles in
+@pytest.mark.parametrize("d,N", [(128, 256), (64, 192)])
+def test_many_small_units(env, d, N, causal):
+    # 256 (batch, head) planes of N rows: 512 units of one to four tiles in
     # each pass, so every CTA runs three or four unit changes (stationary
-    # copies, D shares, dQ staging, accumulator hand-off) back to back
-    run(env, 87, 8, 32, 8, 256, 256, 128, causal)
+    # copies, D shares, dQ staging, accumulator hand-off) back to back; at
+    # d = 64 with N = 192 each plane also ends in a half-filled 128-row tile
+    run(env, 87, 8, 32, 8, N, N, d, causal)
