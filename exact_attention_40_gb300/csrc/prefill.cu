@@ -243,6 +243,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.abort_flag = 0u;
     fence_mbar_init();
   }
+
+  int issued_pairs[2] = {0, 0};    // producer: copy pairs issued per pair slot
+  int q_loads[kQBuf] = {};  // producer: Q tiles issued per buffer
+  bool mma_issued = false;
+  // The CTA's first copies (K_0 and Q_A of its first item: pair 0 in pair
+  // slot 0, Q buffer 0) need no wait, so they go out before the TMEM
+  // allocation and the set-up barrier, whose time their DRAM latency then
+  // overlaps.  early_zk: that item's K/V plane (its V_0 is owed next), or -1.
+  int early_zk = -1;
+  if (warp == kWarpLoad && lane == 0) {
+    const int idx0 = item_index(0);
+    if (idx0 < p.n_items) {
+      const Item it0 = item_at(idx0, p);
+      if (it0.n_iter > 0 && it0.ti[0].n_kv > 0) {
+        const uint64_t keep0 = l2_policy_evict_last();
+        mbar_arrive_expect_tx(&sm.full[0], D * kBN * 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d_hint(sm.ring[0][c], &tm_k, &sm.full[0], c * 64, 0, it0.zk, keep0);
+        issued_pairs[0] = 1;
+        mbar_arrive_expect_tx(&sm.q_full[0], D * kBM * 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm.q[0][c], &tm_q, &sm.q_full[0], c * 64, it0.m0, it0.zq);
+        q_loads[0] = 1;
+        early_zk = it0.zk;
+      }
+    }
+  }
   if (warp == kWarpMma) {
     __syncwarp();
     tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -253,17 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
 
-  int issued_pairs[2] = {0, 0};    // producer: copy pairs issued per pair slot
-  int q_loads[kQBuf] = {};  // producer: Q tiles issued per buffer
-  bool mma_issued = false;
-
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();  // K/V tiles are re-read by other CTAs
-      int g = 0;   // running pair index: pair g uses pair slot g & 1
-      int qt = 0;  // running Q tile index: tile t uses buffer t % kQBuf
-      int v_zk = -1, v_tile = 0;  // the V tile owed by the next pair (v_zk < 0: none)
+      const bool early = early_zk >= 0;  // pair 0 and Q_A of the first item already issued
+      int g = early ? 1 : 0;    // running pair index: pair g uses pair slot g & 1
+      int qt = early ? 1 : 0;   // running Q tile index: tile t uses buffer t % kQBuf
+      int v_zk = early_zk, v_tile = 0;  // the V tile owed by the next pair (v_zk < 0: none)
       bool ok = true;
       // Pair g = {the owed V tile, K tile k_tile of plane k_zk (if k_zk >= 0)};
       // the V tile with the same index as that K tile is owed next, so the
@@ -296,22 +322,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx >= p.n_items) break;
         const Item it = item_at(idx, p);
         if (it.n_iter == 0) continue;
-        // The previous item's last V is needed before this item's Q.
-        if (!(ok = issue_pair(it.zk, 0))) break;
+        // The previous item's last V is needed before this item's Q.  (The
+        // first item's K_0 and Q_A went out before the set-up barrier.)
+        const bool pre = round == 0 && early;
+        if (!pre && !(ok = issue_pair(it.zk, 0))) break;
         for (int x = 0; x < 2; ++x) {
           if (it.ti[x].n_kv == 0) continue;
-          const int b = qt % kQBuf;
-          // the previous Q of this buffer must have been read by its last S
-          if (q_loads[b] > 0 && !wait_or_abort(&sm.q_free[b], (q_loads[b] - 1) & 1, p, &sm.abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.q_full[b], D * kBM * 2);
+          const int b = pre && x == 0 ? 0 : qt % kQBuf;
+          if (!(pre && x == 0)) {
+            // the previous Q of this buffer must have been read by its last S
+            if (q_loads[b] > 0 && !wait_or_abort(&sm.q_free[b], (q_loads[b] - 1) & 1, p, &sm.abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.q_full[b], D * kBM * 2);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sm.q[b][c], &tm_q, &sm.q_full[b], c * 64, it.m0 + x * kBM, it.zq);
-          ++q_loads[b];
-          ++qt;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(sm.q[b][c], &tm_q, &sm.q_full[b], c * 64, it.m0 + x * kBM, it.zq);
+            ++q_loads[b];
+            ++qt;
+          }
           if (round == 0 && x == 0) {
             // the CTA's first S needs only K_0 and Q_A: let them arrive
             // before the rest of the first item's copies share the bandwidth
