@@ -30,9 +30,9 @@
 //              4-slot ring; an item's last V travels with the next item's K_0.
 //   warp 9     tcgen05 issuer (the whole warp runs the loop, one elected
 //              lane issues), also owns the TMEM allocation.
-//   warp 10    issues each staged O tile's TMA store and releases the
-//              staging tile once the copy has read it, so no softmax warp
-//              waits for a store.
+//   warp 10    issues each staged O tile's TMA store and, once the copy has
+//              read the staging tile, hands it to the warpgroup of the
+//              CTA's next O tile, so no softmax warp waits for a store.
 //              Issue order per key tile j:
 //                S_A = Q_A K_j^T,  O_B += P_B(j-1) V_(j-1),  S_B = Q_B K_j^T,
 //                O_A += P_A(j) V_j
@@ -76,7 +76,7 @@ struct alignas(1024) PrefillSmem {
   uint8_t q[kQBuf][D / 64][kSubTileBytes];     // Q tiles, a ring over the CTA's tiles
   uint8_t ring[kRing][D / 64][kSubTileBytes];  // K/V tiles
   uint8_t ostage[D / 64][kSubTileBytes];       // a finished O tile, bf16, as the O tensor map stores it
-  uint64_t stage_free;                    // the staged O tile has been read by its TMA store
+  uint64_t stage_go[2];                   // warpgroup x may stage its next O tile (the previous tile's copy has read it)
   uint64_t staged;                        // the four warps of a tile's warpgroup have staged their rows
   uint64_t q_full[kQBuf], q_free[kQBuf];  // Q tile landed / Q buffer no longer read
   uint64_t full[2], empty[2];  // per pair slot: pair j = {V_(j-1), K_j}
@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
-    mbar_init(&sm.stage_free, 1);
+    mbar_init(&sm.stage_go[0], 1);
+    mbar_init(&sm.stage_go[1], 1);
     mbar_init(&sm.staged, 4);
     for (int b = 0; b < kQBuf; ++b) {
       mbar_init(&sm.q_full[b], 1);
@@ -473,8 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpStore) {
     // ------------------------------------------------------------ O stores
     // The CTA's O tiles in the softmax warpgroups' order (per item, A then
-    // B, tiles that exist): once a tile is staged, one TMA store of it, and
-    // the staging tile is released as soon as the copy has read it.
+    // B, tiles that exist).  Before each tile but the first, the staging
+    // tile (whose previous copy has been read) is handed to that tile's
+    // warpgroup through the warpgroup's own barrier, so each warpgroup
+    // waits for exactly its own hand-overs, in order, however many tiles
+    // of the other warpgroup lie between two of its own (an item without a
+    // tile B gives tile A twice in a row); then one TMA store of the tile.
     if (lane == 0) {
       int e = 0;
       bool ok = true;
@@ -485,12 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 2 && ok; ++x) {
           const int row0 = it.m0 + x * kBM;
           if (row0 >= p.Nq) continue;
+          if (e > 0) mbar_arrive(&sm.stage_go[x]);
           if (!(ok = wait_or_abort(&sm.staged, e & 1, p, &sm.abort_flag))) break;
 #pragma unroll
           for (int sub = 0; sub < D / 64; ++sub) tma_store_3d(&tm_o, sm.ostage[sub], sub * 64, row0, it.zq);
           bulk_commit_group();
           bulk_wait_group_read0();
-          mbar_arrive(&sm.stage_free);
           ++e;
         }
       }
@@ -505,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_o = t_lane + tmem_o_col(x);
     int s_waits = 0, o_waits = 0;
     int e_base = 0;  // O tiles of this CTA's earlier items (the staging buffer's users, in order)
+    int go_waits = 0;  // hand-overs of the staging tile this warpgroup has consumed
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int idx = item_index(round);
@@ -622,9 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse = row_has_keys ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         p.lse[static_cast<size_t>(it.zq) * p.Nq + row] = lse;
       }
-      if (e_tile > 0 &&
-          !__all_sync(0xffffffffu, wait_or_abort(&sm.stage_free, (e_tile - 1) & 1, p, &sm.abort_flag)))
-        break;
+      if (e_tile > 0) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(&sm.stage_go[x], go_waits & 1, p, &sm.abort_flag))) break;
+        ++go_waits;
+      }
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];

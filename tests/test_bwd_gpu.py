@@ -141,3 +141,11 @@ def test_many_small_units(env, d, N, causal):
     # copies, D shares, dQ staging, accumulator hand-off) back to back; at
     # d = 64 with N = 192 each plane also ends in a half-filled 128-row tile
     run(env, 87, 8, 32, 8, N, N, d, causal)
+
+
+def test_empty_units_between_others(env):
+    # Nq - Nk = 256 under the bottom-right causal mask: the first two 128-row
+    # query tiles of every plane see no key, so two thirds of the dQ pass's
+    # 768 units are empty and sit between non-empty ones on the same CTA
+    # (their copies, zero dQ and release run in the same protocol)
+    run(env, 88, 8, 32, 8, 384, 128, 128, True)

@@ -49,6 +49,11 @@ SHAPES = [
     (3, 2, 2, 257, 513, 64, True),
     (1, 16, 2, 384, 384, 128, True),  # GQA group 8
     (2, 2, 2, 640, 640, 128, False),
+    # several items per CTA, some without a tile B (Nq mod 256 <= 128), so
+    # one warpgroup stages two O tiles in a row between the other's
+    (8, 32, 8, 384, 384, 128, False),
+    (8, 32, 8, 384, 128, 128, True),  # and the first item of each head sees no key
+    (8, 16, 4, 328, 328, 64, True),
 ]
 
 
