@@ -54,6 +54,9 @@ SHAPES = [
     (8, 32, 8, 384, 384, 128, False),
     (8, 32, 8, 384, 128, 128, True),  # and the first item of each head sees no key
     (8, 16, 4, 328, 328, 64, True),
+    # Nq - Nk = 150: each head's first item has an empty tile A and a tile B
+    # that sees keys; its second has a tile A only
+    (8, 32, 8, 300, 150, 128, True),
 ]
 
 
