@@ -49,7 +49,10 @@ EDGE_LENS = [1, 15, 16, 17, 511, 512, 513, 1024, 1500, 8192]
 
 
 @pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 8, 128), (8, 4, 64), (16, 2, 128),
-                                      (4, 1, 64)])
+                                      (4, 1, 64),
+                                      # groups of 16, 24 and 32 query heads: one, one and a half
+                                      # and two 16-row chunks per KV head
+                                      (16, 1, 128), (24, 1, 64), (32, 1, 128)])
 def test_edge_lengths(env, Hq, Hkv, d):
     inp = synth.decode_inputs_lens(61, np.array(EDGE_LENS, np.int32), Hq, Hkv, d)
     scale = 1.0 / math.sqrt(d)
