@@ -126,10 +126,10 @@ def test_empty_sides(env):
     assert ex.attn_get_device_status() == 0
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (6, 2), (2, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (6, 2), (2, 2), (32, 2)])
 def test_group_sizes(env, Hq, Hkv):
-    # groups of 8 and 3 (fp32 partials and their sum in head order) and 1
-    # (dK, dV written directly)
+    # groups of 8, 3 and 16 (fp32 partials and their sum in head order) and
+    # 1 (dK, dV written directly)
     run(env, 86, 1, Hq, Hkv, 200, 200, 64, True)
 
 

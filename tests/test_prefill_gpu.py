@@ -48,6 +48,7 @@ SHAPES = [
     (1, 4, 4, 200, 77, 128, True),   # Nq > Nk: the first rows see no key at all
     (3, 2, 2, 257, 513, 64, True),
     (1, 16, 2, 384, 384, 128, True),  # GQA group 8
+    (2, 32, 1, 256, 256, 64, True),   # GQA group 32
     (2, 2, 2, 640, 640, 128, False),
     # several items per CTA, some without a tile B (Nq mod 256 <= 128), so
     # one warpgroup stages two O tiles in a row between the other's
