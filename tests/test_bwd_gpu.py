@@ -149,3 +149,10 @@ def test_empty_units_between_others(env):
     # 768 units are empty and sit between non-empty ones on the same CTA
     # (their copies, zero dQ and release run in the same protocol)
     run(env, 88, 8, 32, 8, 384, 128, 128, True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_one_key_many_queries(env, causal):
+    # 880 queries against one key: dQ units of one tile (or, causal, none
+    # but the last row's), dK/dV units with seven (or one) query tiles
+    run(env, 89, 4, 32, 8, 880, 1, 64, causal)

@@ -58,6 +58,11 @@ SHAPES = [
     # Nq - Nk = 150: each head's first item has an empty tile A and a tile B
     # that sees keys; its second has a tile A only
     (8, 32, 8, 300, 150, 128, True),
+    # one key, 880 queries: four one-key-tile items per head, the last with
+    # a tile A only; causal, only the last row sees the key, so three of
+    # each head's items are empty
+    (4, 32, 8, 880, 1, 64, False),
+    (4, 32, 8, 880, 1, 64, True),
 ]
 
 
