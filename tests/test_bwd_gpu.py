@@ -156,3 +156,10 @@ def test_one_key_many_queries(env, causal):
     # 880 queries against one key: dQ units of one tile (or, causal, none
     # but the last row's), dK/dV units with seven (or one) query tiles
     run(env, 89, 4, 32, 8, 880, 1, 64, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_one_query_many_keys(env, causal):
+    # one query against 4000 keys: 8192 dK/dV units of one query tile each,
+    # about 54 a CTA, back to back
+    run(env, 90, 8, 32, 8, 1, 4000, 128, causal)

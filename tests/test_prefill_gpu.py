@@ -63,6 +63,8 @@ SHAPES = [
     # each head's items are empty
     (4, 32, 8, 880, 1, 64, False),
     (4, 32, 8, 880, 1, 64, True),
+    # one query against 4000 keys: items with a tile A only across 32 key tiles
+    (8, 32, 8, 1, 4000, 128, True),
 ]
 
 
