@@ -65,6 +65,8 @@ SHAPES = [
     (4, 32, 8, 880, 1, 64, True),
     # one query against 4000 keys: items with a tile A only across 32 key tiles
     (8, 32, 8, 1, 4000, 128, True),
+    # d = 64 with several full items per CTA (512 items, causal)
+    (4, 32, 8, 1024, 1024, 64, True),
 ]
 
 
